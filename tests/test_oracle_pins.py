@@ -1,0 +1,308 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself:
+hand-derived values, closed forms, invariants and library routines.
+
+The pages print no worked values, so every pin here is one of: arithmetic done by
+hand from the quantiser's definition, a closed form of the normalisation /
+rotation / attention formulas, an invariant the method guarantees (rotation
+composition, chunked == unchunked softmax, padding and permutation
+invariance), or a special case that reduces to a library routine (numpy matmul
+for dequantised scores, torch's scaled_dot_product_attention for dense causal
+attention).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention, prep_queries, quantize_rows, score, score_abs_bound
+from sparse_selected_attention_gb300 import workloads as wl
+
+# ----------------------------------------------------------------------------
+# quantiser
+# ----------------------------------------------------------------------------
+
+
+def _group(vals, n=32):
+    g = np.zeros(n, dtype=np.float32)
+    g[: len(vals)] = vals
+    return g
+
+
+def test_quantize_unit_scale_rounds_half_to_even():
+    # amax = 127 -> 127/127 = 1.0 exactly -> fp16 1.0; codes are rint(x) with
+    # ties to even, then the clamp.
+    x = _group([127.0, 2.5, 3.5, -2.5, -3.5, 0.5, 1.5, -127.0, 126.5, -0.5, 0.49999997])
+    codes, scales = quantize_rows(x[None, :])
+    assert scales.dtype == np.float16 and float(scales[0, 0]) == 1.0
+    assert codes[0, :11].tolist() == [127, 2, 4, -2, -4, 0, 2, -127, 126, 0, 0]
+    assert not codes[0, 11:].any()
+
+
+def test_quantize_scale_is_fp16_of_fp32_quotient_and_divides_by_stored_scale():
+    # amax = 1: 1/127 = 0.0078740157..., between 2^-7 and 2^-6; the fp16
+    # significand is round(1.0078740 * 1024) = 1032 -> scale = 1032 * 2^-17
+    # = 0.00787353515625 (bits 0x2008).
+    s = 1032 * 2.0 ** -17
+    x = _group([1.0,
+                516 * 2.0 ** -17,     # x / s = 0.5 exactly -> 0 (tie to even)
+                1548 * 2.0 ** -17,    # x / s = 1.5 exactly -> 2
+                -0.25,                # -31.7505... -> -32
+                0.79132])             # / stored scale = 100.5038 -> 101
+                                      # (/ unrounded 1/127 would be 100.4976 -> 100)
+    codes, scales = quantize_rows(x[None, :])
+    assert int(scales.view(np.uint16)[0, 0]) == 0x2008
+    assert float(scales[0, 0]) == s
+    assert codes[0, :5].tolist() == [127, 0, 2, -32, 101]
+
+
+def test_quantize_zero_group_and_subnormal_scale():
+    x = np.zeros((1, 128), dtype=np.float32)
+    # group 1: amax = 127 * 2^-20 -> scale 2^-20 (an fp16 subnormal, exact).
+    x[0, 32] = 127 * 2.0 ** -20
+    x[0, 33] = 3.5 * 2.0 ** -20      # -> 4
+    x[0, 34] = -2.5 * 2.0 ** -20     # -> -2
+    # group 2: a negative maximum maps to -127.
+    x[0, 64] = -3.0
+    x[0, 65] = 1.5                   # 1.5 / fp16(3/127) -> 63.5... -> 64 (see below)
+    codes, scales = quantize_rows(x)
+    assert float(scales[0, 0]) == 0.0 and not codes[0, :32].any()
+    assert float(scales[0, 1]) == 2.0 ** -20
+    assert codes[0, 32:35].tolist() == [127, 4, -2]
+    assert codes[0, 64] == -127
+    # 3/127 = 0.0236220..., fp16 significand round(1.511811 * 1024) = 1548
+    # -> 1548 * 2^-16 = 0.02362060546875; 1.5 / that = 63.5039 -> 64.
+    assert float(scales[0, 2]) == 1548 * 2.0 ** -16
+    assert codes[0, 65] == 64
+    assert float(scales[0, 3]) == 0.0
+
+
+def test_quantize_invariants_random():
+    x = (wl.normal(11, 1, (257, 128)) * wl.uniform(11, 2, (257, 1), 1e-3, 30.0)).astype(np.float32)
+    codes, scales = quantize_rows(x)
+    assert codes.dtype == np.int8 and codes.min() >= -127 and codes.max() <= 127
+    sf = np.repeat(scales.astype(np.float64), 32, axis=1)
+    err = np.abs(x.astype(np.float64) - codes.astype(np.float64) * sf)
+    # Round trip within half a step (plus the float32 quotient's rounding,
+    # at most 127 * 2^-24 of a step).
+    assert np.all(err <= sf * (0.5 + 1e-5))
+    # Every group's largest magnitude maps to +-127: the fp16 scale is within
+    # 2^-11 relative of amax/127, so amax/scale is within 0.07 of 127.
+    xg = np.abs(x.reshape(257, 4, 32))
+    cg = np.abs(codes.reshape(257, 4, 32).astype(np.int32))
+    at_max = np.take_along_axis(cg, xg.argmax(-1)[..., None], -1)[..., 0]
+    assert np.all(at_max == 127)
+
+
+# ----------------------------------------------------------------------------
+# query RMS-norm + rotation
+# ----------------------------------------------------------------------------
+
+
+def test_prep_constant_row_closed_form():
+    c, eps = 0.37, 1e-6
+    x = np.full((1, 1, 128), c, dtype=np.float32)
+    g = wl.uniform(3, 1, (128,), 0.5, 1.5).astype(np.float32)
+    y, _, _ = prep_queries(x, g, pos0=0, eps=eps)
+    cf = float(np.float32(c))
+    want = g.astype(np.float64) * cf / math.sqrt(cf * cf + eps)
+    np.testing.assert_allclose(y[0, 0], want, rtol=1e-14)
+
+
+@pytest.mark.parametrize("p", [1, 2, 3, 1000, 31983])
+def test_prep_one_hot_rotates_by_position(p):
+    # x = e_0 (or e_1, e_100), g = 1, eps = 0 -> rs * x = sqrt(128) e_i.
+    g = np.ones(128, dtype=np.float32)
+    for i, f in ((0, 1.0), (1, float(np.float32(10000.0 ** (-2.0 / 64))))):
+        x = np.zeros((1, 1, 128), dtype=np.float32)
+        x[0, 0, i] = 1.0
+        y, _, _ = prep_queries(x, g, pos0=p, eps=0.0)
+        r = math.sqrt(128.0)
+        want = np.zeros(128)
+        want[i] = r * math.cos(p * f)
+        want[i + 32] = r * math.sin(p * f)
+        np.testing.assert_allclose(y[0, 0], want, atol=1e-12)
+    x = np.zeros((1, 1, 128), dtype=np.float32)
+    x[0, 0, 100] = 1.0
+    y, _, _ = prep_queries(x, g, pos0=p, eps=0.0)
+    want = np.zeros(128)
+    want[100] = math.sqrt(128.0)
+    np.testing.assert_allclose(y[0, 0], want, atol=1e-12)
+
+
+def test_prep_rotation_preserves_pair_norms_and_composes():
+    inp = wl.prep_inputs(3, seed=9)
+    ones = np.ones(128, dtype=np.float32)
+    y0, _, _ = prep_queries(inp.q_in, inp.norm_w, pos0=0)
+    y1, _, _ = prep_queries(inp.q_in, inp.norm_w, pos0=12345)
+    n0 = y0[..., :32] ** 2 + y0[..., 32:64] ** 2
+    n1 = y1[..., :32] ** 2 + y1[..., 32:64] ** 2
+    np.testing.assert_allclose(n1, n0, rtol=1e-12)
+    np.testing.assert_array_equal(y1[..., 64:], y0[..., 64:])
+    # With g = 1 and eps = 0 the normalised row has unit RMS, so normalising
+    # again is the identity and rotations by p1 then p2 equal one by p1 + p2.
+    a, _, _ = prep_queries(inp.q_in, ones, pos0=700, eps=0.0)
+    b, _, _ = prep_queries(a.astype(np.float32), ones, pos0=2100, eps=0.0)
+    c, _, _ = prep_queries(inp.q_in, ones, pos0=2800, eps=0.0)
+    # Token t is at position pos0 + t in each call, so compare token 0 only.
+    np.testing.assert_allclose(b[0], c[0], atol=2e-6)
+
+
+# ----------------------------------------------------------------------------
+# score
+# ----------------------------------------------------------------------------
+
+
+def test_score_one_hot_query_closed_form():
+    cache = wl.make_cache(300, seed=4)
+    q = np.zeros((2, 12, 128), dtype=np.float32)
+    q[0, 7, 77] = 1.0           # group 2
+    q[1, 0, 5] = -2.0           # group 0
+    S = score(q, cache.kq, cache.ksc, pos0=250)
+    c = np.arange(251)
+    np.testing.assert_array_equal(S[0, :251], cache.ksc[c, 2].astype(np.float64) * cache.kq[c, 77])
+    np.testing.assert_array_equal(S[1, :252], -2.0 * cache.ksc[:252, 0].astype(np.float64) * cache.kq[:252, 5])
+    assert np.all(np.isnan(S[0, 251:])) and np.all(np.isnan(S[1, 252:]))
+
+
+def test_score_equals_dense_matmul_on_dequantised_keys_and_is_head_linear():
+    cache = wl.make_cache(400, seed=6)
+    cache.ksc[17] = 0                               # a dead key row
+    q = wl.queries_f32(40, seed=6)
+    S = score(q, cache.kq, cache.ksc, pos0=360)
+    kdq = cache.kq.astype(np.float64) * np.repeat(cache.ksc.astype(np.float64), 32, axis=1)
+    dense = q.astype(np.float64).sum(axis=1) @ kdq.T
+    causal = np.arange(400)[None, :] <= (360 + np.arange(40))[:, None]
+    np.testing.assert_allclose(S[causal], dense[causal], rtol=1e-12, atol=1e-12)
+    assert np.all(S[:, 17] == 0.0)
+    # All heads equal -> 12x the one-head score.
+    q1 = np.repeat(q[:, :1], 12, axis=1)
+    S12 = score(q1, cache.kq, cache.ksc, pos0=360)
+    S1 = score(q[:, :1], cache.kq, cache.ksc, pos0=360)
+    np.testing.assert_allclose(S12[causal], 12.0 * S1[causal], rtol=1e-12, atol=1e-12)
+    A = score_abs_bound(q, cache.kq, cache.ksc, pos0=360)
+    assert np.all(np.abs(S[causal]) <= A[causal] * (1 + 1e-12))
+
+
+# ----------------------------------------------------------------------------
+# attention
+# ----------------------------------------------------------------------------
+
+SCALE = 1.0 / math.sqrt(128.0)
+
+
+def _dequant(cache):
+    k = cache.kq.astype(np.float64) * np.repeat(cache.ksc.astype(np.float64), 32, axis=1)
+    v = cache.vq.astype(np.float64) * np.repeat(cache.vsc.astype(np.float64), 32, axis=1)
+    return k, v
+
+
+def _softmax_attn(q, k, v, cells, weights=None):
+    """Textbook single softmax over the listed cells (float64)."""
+    s = SCALE * (q.astype(np.float64) @ k[cells].T)            # [H, n]
+    s = s - s.max(axis=1, keepdims=True)
+    e = np.exp(s) * (1.0 if weights is None else weights[None, :])
+    return (e @ v[cells]) / e.sum(axis=1, keepdims=True)
+
+
+def test_attention_width_one_is_the_dequantised_value_row():
+    cache = wl.make_cache(50, seed=2)
+    q = wl.queries_f16(3, seed=2)
+    ids = np.full((3, 64), -1, dtype=np.int32)
+    ids[0, 0], ids[1, 63], ids[2, 17] = 5, 49, 0
+    out64, out16, _, bad = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, ids, SCALE)
+    _, v = _dequant(cache)
+    for t, c in enumerate([5, 49, 0]):
+        np.testing.assert_array_equal(out64[t], np.broadcast_to(v[c], (12, 128)))
+        np.testing.assert_array_equal(out16[t], np.broadcast_to(v[c], (12, 128)).astype(np.float16))
+    assert not bad
+
+
+def test_attention_equal_scores_give_the_plain_mean():
+    cache = wl.make_cache(700, seed=8)
+    q = np.zeros((2, 12, 128), dtype=np.float16)
+    q[1] = np.float16(-0.0)
+    ids = wl.even_ids(2, 698, width=704, select=650)
+    out64, _, _, _ = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, ids, SCALE)
+    _, v = _dequant(cache)
+    for t in range(2):
+        cells = ids[t][ids[t] >= 0]
+        np.testing.assert_allclose(out64[t], np.broadcast_to(v[cells].mean(axis=0), (12, 128)), rtol=1e-12, atol=1e-15)
+
+
+def test_attention_contiguous_ids_equal_dense_causal_sdpa():
+    T, pos0 = 70, 100
+    cache = wl.make_cache(pos0 + T, seed=12)
+    q = wl.queries_f16(T, seed=12)
+    ids = wl.even_ids(T, pos0, width=192, select=4096)   # all cells 0..p
+    out64, _, _, _ = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, ids, SCALE)
+    k, v = _dequant(cache)
+    Q = torch.from_numpy(q.astype(np.float64)).permute(1, 0, 2)[None]       # [1, H, T, D]
+    K = torch.from_numpy(k)[None, None].expand(1, 12, -1, -1)
+    V = torch.from_numpy(v)[None, None].expand(1, 12, -1, -1)
+    mask = torch.arange(pos0 + T)[None, :] <= (pos0 + torch.arange(T))[:, None]
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=SCALE)
+    np.testing.assert_allclose(out64, ref[0].permute(1, 0, 2).numpy(), rtol=1e-11, atol=1e-14)
+
+
+def test_attention_chunked_merge_equals_single_softmax_for_arbitrary_ids():
+    cache = wl.make_cache(5000, seed=13)
+    q = wl.queries_f16(6, seed=13)
+    k, v = _dequant(cache)
+    rng = np.random.default_rng(13)
+    ids = np.full((6, 448), -1, dtype=np.int32)
+    for t in range(6):
+        n = int(rng.integers(1, 448))
+        ids[t, :n] = rng.choice(5000, size=n, replace=False)
+    out64, _, _, _ = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, ids, SCALE)
+    for t in range(6):
+        cells = ids[t][ids[t] >= 0]
+        np.testing.assert_allclose(out64[t], _softmax_attn(q[t], k, v, cells), rtol=1e-11, atol=1e-14)
+
+
+def test_attention_padding_permutation_and_duplication():
+    cache = wl.make_cache(3000, seed=14)
+    q = wl.queries_f16(1, seed=14)
+    k, v = _dequant(cache)
+    base = np.full((1, 320), -1, dtype=np.int32)
+    cells = np.arange(2, 3000, 11)[:250].astype(np.int32)
+    base[0, :250] = cells
+    ref, _, _, _ = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, base, SCALE)
+    # -1 slots inserted anywhere (whole chunks too) leave the result unchanged.
+    padded = np.full((1, 640), -1, dtype=np.int32)
+    pos = np.sort(np.random.default_rng(1).choice(np.arange(64, 640), size=250, replace=False))
+    padded[0, pos] = cells
+    out, _, _, _ = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, padded, SCALE)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-15)
+    # A permutation of the list changes nothing.
+    perm = base.copy()
+    perm[0, :250] = np.random.default_rng(2).permutation(cells)
+    out, _, _, _ = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, perm, SCALE)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-15)
+    # A duplicated id counts twice: softmax with weight 2 on that cell.
+    dup = base.copy()
+    dup[0, 250] = cells[40]
+    out, _, _, _ = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, dup, SCALE)
+    w = np.ones(250)
+    w[40] = 2.0
+    np.testing.assert_allclose(out[0], _softmax_attn(q[0], k, v, cells, w), rtol=1e-11, atol=1e-14)
+
+
+def test_attention_part_and_empty_and_bad_ids():
+    cache = wl.make_cache(200, seed=15)
+    q = wl.queries_f16(3, seed=15)
+    ids = np.full((3, 128), -1, dtype=np.int32)
+    ids[0, :64] = np.arange(64)            # one full chunk, second chunk empty
+    ids[2, 70] = 500                        # out of range -> padding + flag
+    ids[2, 71] = -7                         # below -1 -> padding + flag
+    ids[2, 72] = 3
+    out64, out16, part, bad = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, ids, SCALE, want_part=True)
+    assert bad
+    assert np.all(out16[1] == 0) and not np.signbit(out16[1]).any()
+    k, v = _dequant(cache)
+    s = SCALE * (q[0].astype(np.float64) @ k[:64].T)
+    np.testing.assert_allclose(part[0, 0, :, 128], s.max(axis=1), rtol=1e-13)
+    np.testing.assert_allclose(part[0, 0, :, :128] / part[0, 0, :, 129:130], out64[0], rtol=1e-12)
+    assert np.all(part[0, 1, :, 128] == -np.inf) and np.all(part[0, 1, :, 129] == 0)
+    _, vv = _dequant(cache)
+    np.testing.assert_array_equal(out64[2], np.broadcast_to(vv[3], (12, 128)))
