@@ -1,0 +1,389 @@
+"""Benchmark of the QSA hot path: one step = qsa_prep + qsa_score + qsa_attn.
+
+Workload: prompt attention, long context -- T = 1984 query tokens at
+pos0 = 30000 over a 31984-cell int8 K/V cache (fp16 scales per 32 dims),
+12 query heads sharing one KV head, head_dim 128, 2048 evenly spaced causal
+selected ids per token (W = 2048).  The step normalises/rotates the queries
+and quantises the new K/V rows into the cache, scores every causal cell
+(fp32 queries, 61.5 M scores written) and runs the selected-id attention.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "query tokens/s and achieved HBM GB/s (% of roofline) for QSA attention at T=1984"
+UNIT = "tokens/s"
+NTOK, POS0, WIDTH, HQ, D, G = 1984, 30000, 2048, 12, 128, 32
+WORKLOAD = ("prompt attention long context: T=1984 query tokens, pos0=30000, int8 K/V cache of 31984 cells "
+            "with fp16 per-32 scales, 12 q heads / 1 KV head, head_dim 128, 2048 evenly spaced causal ids per "
+            "token; step = qsa_prep + qsa_score (fp32 q, all causal cells) + qsa_attn")
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+KERNELS = ("prep", "score", "attn")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--ntok", type=int, default=NTOK, help="fewer tokens: for small profiling captures only")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-sample-seconds", type=float, default=15.0)
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work per launch (bytes the method must move, flops it must do)
+# ---------------------------------------------------------------------------
+
+def attn_bytes(ids_np, ntok):
+    """Gathered bytes: per valid id 2 * (D + 2*D/G) = 272 B (K and V codes plus
+    scales), every id slot read (4 B), q read and out written (fp16)."""
+    valid = int((ids_np >= 0).sum())
+    return valid * 2 * (D + 2 * (D // G)) + ids_np.size * 4 + 2 * ntok * HQ * D * 2, valid
+
+
+def score_pairs(ntok, pos0):
+    return sum(pos0 + t + 1 for t in range(ntok))
+
+
+def score_bytes(ntok, pos0, cells):
+    """fp32 q read, int8 codes + fp16 scales of every cell read, one fp32 score
+    written per causal (token, cell) pair."""
+    return ntok * HQ * D * 4 + cells * (D + 2 * (D // G)) + 4 * score_pairs(ntok, pos0)
+
+
+def prep_bytes(ntok):
+    return ntok * HQ * D * (4 + 2 + 4) + 2 * ntok * D * 4 + 2 * ntok * (D + 2 * (D // G)) + D * 4
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
+
+
+def traffic_record(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; None otherwise."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+    except Exception:
+        return None
+    src = os.path.join(ROOT, "sparse_selected_attention_gb300", "csrc", rec["source"])
+    try:
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
+                return None
+    except OSError:
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample
+# ---------------------------------------------------------------------------
+
+CPU_SAMPLE_CODE = r"""
+import json, math, sys, time
+sys.path.insert(0, ROOT)
+import numpy as np
+from oracle import attention, prep, score
+from sparse_selected_attention_gb300 import workloads as wl
+n = NSAMP
+T, pos0 = 1984, 30000
+inp = wl.prep_inputs(T, seed=5)
+cache = wl.make_cache(pos0 + T, seed=5)
+ids = wl.even_ids(T, pos0)
+rows = np.linspace(0, T - 1, n).astype(np.int64)
+t0 = time.perf_counter()
+q64, q16, q32 = prep(inp.q_in[rows], inp.k_in[rows], inp.v_in[rows], inp.norm_w, pos0, cache.kq, cache.vq,
+                     cache.ksc, cache.vsc)
+S = score(q32, cache.kq, cache.ksc, pos0)
+o = attention(q16, cache.kq, cache.vq, cache.ksc, cache.vsc, ids[rows], 1 / math.sqrt(128))
+dt = time.perf_counter() - t0
+print(json.dumps({"tokens": n, "seconds": dt}))
+"""
+
+
+def run_cpu_sample(nsamp):
+    code = CPU_SAMPLE_CODE.replace("ROOT", repr(ROOT)).replace("NSAMP", str(nsamp))
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(target_seconds):
+    probe = run_cpu_sample(4)
+    per_tok = probe["seconds"] / 4
+    n = int(max(4, min(1984, target_seconds / max(per_tok, 1e-6))))
+    res = run_cpu_sample(n)
+    return {"value": res["tokens"] / res["seconds"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{res['tokens']} evenly spaced token rows of the workload (prep of their rows, their "
+                      f"score rows over all causal cells, their attention), {res['seconds']:.1f} s, one thread"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    from sparse_selected_attention_gb300 import (qsa_attn, qsa_prep, qsa_score, qsa_score_workspace_bytes)
+    from sparse_selected_attention_gb300 import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    T, pos0 = args.ntok, POS0
+    C = pos0 + T
+    inp = wl.prep_inputs(T, seed=5 + rank)
+    cache = wl.make_cache(C, seed=5 + rank)
+    ids_np = wl.even_ids(T, pos0, WIDTH)
+
+    def d(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+    q_in, k_in, v_in, norm_w = d(inp.q_in), d(inp.k_in), d(inp.v_in), d(inp.norm_w)
+    kq, vq, ksc, vsc = d(cache.kq), d(cache.vq), d(cache.ksc), d(cache.vsc)
+    ids = d(ids_np)
+    q16 = torch.empty((T, HQ, D), dtype=torch.float16, device=dev)
+    q32 = torch.empty((T, HQ, D), dtype=torch.float32, device=dev)
+    scores = torch.empty((T, C), dtype=torch.float32, device=dev)
+    ws = torch.empty(qsa_score_workspace_bytes(T), dtype=torch.uint8, device=dev)
+    out = torch.empty((T, HQ, D), dtype=torch.float16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        qsa_prep(q_in, k_in, v_in, norm_w, pos0, kq, vq, ksc, vsc, q16, q_out_f32=q32)
+        if ev:
+            ev[1].record(stream)
+        qsa_score(q32, kq, ksc, pos0, scores, ws)
+        if ev:
+            ev[2].record(stream)
+        qsa_attn(q16, kq, vq, ksc, vsc, ids, out)
+        if ev:
+            ev[3].record(stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    barrier()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    wall0 = time.perf_counter()
+    for k in range(K):
+        flush.zero_()  # L2 flush between steps, outside the step's events
+        step(evs[k])
+    barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    per = {n: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)] for i, n in enumerate(KERNELS)}
+    step_ms = [evs[k][0].elapsed_time(evs[k][3]) for k in range(K)]
+    ms = sum(step_ms) / K
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # End to end through the public API: H2D of the step's inputs from pinned
+    # host memory, the three calls, D2H of the attention output.
+    e2e = None
+    if not args.no_e2e:
+        h_q, h_k, h_v = (torch.from_numpy(x).pin_memory() for x in (inp.q_in, inp.k_in, inp.v_in))
+        h_ids = torch.from_numpy(ids_np).pin_memory()
+        h_out = torch.empty((T, HQ, D), dtype=torch.float16).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_ids))
+        d2h = h_out.numel() * h_out.element_size()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def e2e_step():
+            q_in.copy_(h_q, non_blocking=True)
+            k_in.copy_(h_k, non_blocking=True)
+            v_in.copy_(h_v, non_blocking=True)
+            ids.copy_(h_ids, non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            flush.zero_()
+            e2e_step()
+        tot = 0.0
+        for _ in range(K):
+            flush.zero_()
+            e0.record(stream)
+            e2e_step()
+            e1.record(stream)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1)
+        e2e_ms = tot / K
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    # Roofline of the dominant kernel.
+    avg = {n: sum(v) / K for n, v in per.items()}
+    dom = max(avg, key=avg.get)
+    ab, valid = attn_bytes(ids_np, T)
+    alg = {"attn": ab, "score": score_bytes(T, pos0, C), "prep": prep_bytes(T)}
+    peak, peak_src = peaks()
+    achieved = alg[dom] / (avg[dom] / 1e3) / 1e9
+    src = {"attn": "attn.cu", "score": "score.cu", "prep": "prep.cu"}[dom]
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic_record(dom), "kernel": dom, "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": alg[dom], "avg_launch_ms": avg[dom]}
+    kernels = {n: {"avg_ms": avg[n], "algorithmic_bytes": alg[n],
+                   "achieved_gbs": alg[n] / (avg[n] / 1e3) / 1e9} for n in KERNELS}
+    kernels["score"]["pairs"] = score_pairs(T, pos0)
+    kernels["score"]["tflops_algorithmic"] = 2 * HQ * D * score_pairs(T, pos0) / (avg["score"] / 1e3) / 1e12
+    kernels["attn"]["valid_cells"] = valid
+    return {"ms": ms, "wall_s": wall, "e2e": e2e, "clocks": clocks, "roofline": roof, "kernels": kernels,
+            "launches_per_step": 4}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    config = {"workload": WORKLOAD, "ntok": args.ntok, "pos0": POS0, "cache_cells": POS0 + args.ntok,
+              "width": WIDTH, "heads": "12 query / 1 KV", "head_dim": D,
+              "l2": "flushed between steps (256 MiB write), flush outside the step events",
+              "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        cb = cpu_baseline(args.cpu_sample_seconds)
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"] * 1.0, "unit": UNIT, "n_gpus": 0,
+                "steps": 1, "warmup": 0, "ms_per_step": 1e3 * args.ntok / cb["value"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    res = run_ours(args, rank, world, local_rank)
+    if rank != 0:
+        return
+    cb = None
+    if not args.no_cpu_baseline:
+        cb = cpu_baseline(args.cpu_sample_seconds)
+    line = {"metric": METRIC, "value": world * args.ntok / (res["ms"] / 1e3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "precision": "int8 K/V codes with fp16 scales; fp16 tensor-core operands, fp32 accumulation; "
+                         "fp32 prep and scores; fp16 attention output",
+            "data": "synthetic", "config": config, "roofline": res["roofline"], "cpu_baseline": cb,
+            "e2e": res["e2e"], "clocks": res["clocks"], "gpu_launches": res["launches_per_step"] * args.steps,
+            "kernels": res["kernels"]}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

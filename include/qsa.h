@@ -1,0 +1,178 @@
+/*
+ * qsa.h -- C ABI of the QSA attention hot path for NVIDIA GB300 (sm_103a).
+ *
+ * The path has three steps, named after the kernels of the audit pages on
+ * sparse selected attention:
+ *   qsa_prep   query RMS-norm + RoPE, K/V int8 quantisation into the cache;
+ *   qsa_score  head-reduced fp32 scores of every causal cache cell;
+ *   qsa_attn   chunked attention over a per-token list of selected cell ids.
+ *
+ * Conventions shared by every entry point:
+ *  - All buffer pointers in the argument structs are DEVICE pointers owned by
+ *    the caller.  The library allocates nothing and keeps no state between
+ *    calls; it only reads the structs during the call.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL means the legacy default stream).  A QSA_OK return means the
+ *    arguments were accepted and the kernels were enqueued.
+ *  - Argument errors are detected on the host before anything is enqueued and
+ *    are returned synchronously (QSA_ERR_INVALID_ARG, QSA_ERR_UNSUPPORTED).
+ *    Argument validation makes no CUDA call.
+ *  - Conditions only the device can see (an id outside [-1, cache_cells), a
+ *    bounded wait that gave up) set bits (QSA_DEVERR_*) in the caller's
+ *    optional device word `err` with atomicOr; read it after synchronising.
+ *  - Outputs are never pre-cleared: cells a call does not define (scores
+ *    beyond the causal boundary) keep whatever the caller put there.
+ *  - fp16 values are passed as uint16_t bit patterns (IEEE binary16).
+ *  - No C++ exception crosses this boundary.
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QSA_ABI_VERSION 1
+
+typedef enum {
+    QSA_OK = 0,
+    QSA_ERR_INVALID_ARG = 1,  /* null or misaligned pointer, bad size, bad dtype */
+    QSA_ERR_UNSUPPORTED = 2,  /* a shape outside the built kernels (heads, head_dim, group) */
+    QSA_ERR_CUDA = 3          /* a CUDA runtime call or launch failed; see qsa_last_error() */
+} qsa_status;
+
+/* Bits of the device error word. */
+#define QSA_DEVERR_BAD_ID 1u   /* an id < -1 or >= cache_cells was seen and treated as padding */
+#define QSA_DEVERR_TIMEOUT 2u  /* a bounded wait gave up; that launch's outputs are incomplete */
+
+typedef enum { QSA_F32 = 0, QSA_F16 = 1 } qsa_dtype;
+
+/*
+ * qsa_prep -- "Round 36 Track C: qsa_prep Single-Barrier norm_rope & w == 128
+ * tg_sum + qsa_score_mm Loop Unrolling", section "Summary & Decision": the
+ * prep kernel normalises the query rows (RMS reduction, scale rs, weight g),
+ * rotates the dims below QROT against partner tid ^ 32, and writes int8 K/V
+ * codes kq, vq with their scales ksc, vsc ("round 11 track b: qsa attention
+ * and score", "implementation and evaluator": four scale groups per row).
+ *
+ * For token t (position p = pos0 + t) and query head h, with x = q_in[t,h,:]:
+ *   rs = 1/sqrt(mean(x^2) + eps);  y = (rs*x)*norm_w
+ *   for i < rope_dims/2, a = p * fp32(rope_theta^(-2i/rope_dims)):
+ *     y'[i] = y[i] cos a - y[i+rope_dims/2] sin a
+ *     y'[i+rope_dims/2] = y[i+rope_dims/2] cos a + y[i] sin a
+ *   q_out[t,h,:] = fp16_rne(y');  q_out_f32[t,h,:] = y' (if non-NULL)
+ * K and V rows t are quantised into cache row pos0 + t, per group of `group`
+ * dims: s = fp16_rne(fp32(amax/127)); code = s == 0 ? 0 :
+ * clamp(rint_half_even(fp32(x / s)), -127, 127).  Bit-exact by definition.
+ *
+ * Layouts (row-major, contiguous): q_in [ntok, n_q_heads, head_dim] fp32;
+ * k_in, v_in [ntok, n_kv_heads, head_dim] fp32; norm_w [head_dim] fp32;
+ * q_out [ntok, n_q_heads, head_dim] fp16; q_out_f32 same shape fp32 or NULL;
+ * kq, vq [cache_cells, head_dim] int8; ksc, vsc [cache_cells, head_dim/group]
+ * fp16.  Requires pos0 + ntok <= cache_cells.  Supported: n_kv_heads == 1,
+ * head_dim == 128, group == 32, 1 <= n_q_heads <= 30, rope_dims a multiple
+ * of 8 in [0, head_dim].  Float pointers and kq/vq must be 16-byte aligned.
+ */
+typedef struct {
+    int ntok, pos0, n_q_heads, n_kv_heads, head_dim, group, rope_dims, cache_cells;
+    float eps, rope_theta;
+    const float *q_in, *k_in, *v_in, *norm_w;
+    uint16_t *q_out;
+    float *q_out_f32;
+    int8_t *kq, *vq;
+    uint16_t *ksc, *vsc;
+} qsa_prep_args;
+
+/*
+ * qsa_score -- "Round 36 Track C ..." section "Summary & Decision" (the
+ * qsa_score_mm 64x64x128 tile matmul of queries against the int8 key cache)
+ * and "round 11 track b: qsa attention and score", sections "implementation
+ * and evaluator" and "score: valid negative result" (head-reduced output,
+ * scalar dead-key tail, untouched beyond-causal cells).
+ *
+ *   scores[t*ld + c] = sum_h sum_g ksc[c,g] * sum_{d in g} q[t,h,d] * kq[c,d]
+ * for 0 <= c <= pos0 + t; every other element of `scores` is left untouched.
+ *
+ * q: [ntok, n_q_heads, head_dim] in q_dtype (QSA_F32 or QSA_F16).
+ * kq [cache_cells, head_dim] int8, ksc [cache_cells, head_dim/group] fp16.
+ * scores: fp32, row stride ld (elements), ld >= pos0 + ntok.
+ * workspace: device scratch of at least qsa_score_workspace_bytes(ntok,
+ * head_dim) bytes, 256-byte aligned; the call overwrites it.  Two calls that
+ * share a workspace must not run concurrently.
+ * Requires pos0 + ntok <= cache_cells.  Supported: head_dim == 128,
+ * group == 32, 1 <= n_q_heads <= 64.  q, kq 16-byte aligned; ksc 8-byte.
+ */
+typedef struct {
+    int ntok, pos0, n_q_heads, head_dim, group, cache_cells;
+    const void *q;
+    int q_dtype;
+    const int8_t *kq;
+    const uint16_t *ksc;
+    float *scores;
+    int64_t ld;
+    void *workspace;
+    size_t workspace_bytes;
+    unsigned int *err;
+} qsa_score_args;
+
+/* Bytes of workspace qsa_score needs for `ntok` tokens (0 on bad input). */
+size_t qsa_score_workspace_bytes(int ntok, int head_dim);
+
+/*
+ * qsa_attn -- "round 11 track b: qsa attention and score", section
+ * "implementation and evaluator" (per-token selected ids, -1 padding, 64-cell
+ * chunks, incomplete chunks) and "round 5 track b: cached residual norms and
+ * fused mtp attention", sections "mtp attention" and "preflight / ownership"
+ * (per-chunk maxima and denominators, max-first chunk merge, one value load
+ * per dimension per cell shared by all query heads).
+ *
+ * For token t and head h, chunk c covers id slots 64c .. 64c+63; a slot is
+ * valid when 0 <= id < cache_cells (ids < -1 or >= cache_cells are treated
+ * as padding and set QSA_DEVERR_BAD_ID).
+ *   s_j = softmax_scale * sum_g ksc[id,g] * sum_{d in g} q[t,h,d] * kq[id,d]
+ *   m_c = max s_j, l_c = sum exp(s_j - m_c), o_c = sum exp(s_j - m_c) v_j
+ *   with v_j[d] = vsc[id, d/group] * vq[id, d];
+ *   out = fp16(sum_c exp(m_c - M) o_c / sum_c exp(m_c - M) l_c), M = max m_c.
+ * A token with no valid slot outputs +0.
+ *
+ * q [ntok, n_q_heads, head_dim] fp16; ids [ntok, width] int32, width a
+ * multiple of 64; out [ntok, n_q_heads, head_dim] fp16.
+ * part: NULL, or [ntok, width/64, n_q_heads, head_dim + 2] fp32 receiving each
+ * chunk's (o_c[0..head_dim), m_c, l_c); an empty chunk gives (0, -inf, 0).
+ * A non-NULL part selects the split path (per-chunk kernel, then a merge
+ * kernel that reads part back); NULL selects the fused single-kernel path.
+ * Supported: n_kv_heads == 1, head_dim == 128, group == 32,
+ * 1 <= n_q_heads <= 16.  q, kq, vq, out, part 16-byte aligned; ksc, vsc
+ * 8-byte; ids 4-byte.
+ */
+typedef struct {
+    int ntok, n_q_heads, n_kv_heads, head_dim, group, cache_cells, width;
+    const uint16_t *q;
+    const int8_t *kq, *vq;
+    const uint16_t *ksc, *vsc;
+    const int32_t *ids;
+    float softmax_scale;
+    uint16_t *out;
+    float *part;
+    unsigned int *err;
+} qsa_attn_args;
+
+qsa_status qsa_prep(const qsa_prep_args *args, void *stream);
+qsa_status qsa_score(const qsa_score_args *args, void *stream);
+qsa_status qsa_attn(const qsa_attn_args *args, void *stream);
+
+/* Static description of a status code. */
+const char *qsa_status_str(qsa_status s);
+/* Message of the last QSA_ERR_* returned on this host thread ("" if none). */
+const char *qsa_last_error(void);
+/* QSA_ABI_VERSION of the built library. */
+int qsa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H */

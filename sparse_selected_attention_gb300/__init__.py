@@ -1,0 +1,107 @@
+"""GB300-native QSA (sparse selected attention) hot path.
+
+Python binding of the C ABI in include/qsa.h: each function marshals torch
+CUDA tensors into the argument struct and calls the library on the current
+CUDA stream.  All computation runs in libqsa.so's kernels; tensors on the CPU
+are rejected rather than computed elsewhere.
+
+    qsa_prep   query RMS-norm + RoPE, K/V int8 quantisation into the cache
+    qsa_score  head-reduced fp32 scores of every causal cache cell
+    qsa_attn   chunked attention over per-token selected cell ids
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+from . import _abi
+from ._abi import (QSA_DEVERR_BAD_ID, QSA_DEVERR_TIMEOUT, QSAError, lib)  # noqa: F401
+
+__all__ = ["qsa_prep", "qsa_score", "qsa_attn", "qsa_score_workspace_bytes", "qsa_abi_version",
+           "QSAError", "QSA_DEVERR_BAD_ID", "QSA_DEVERR_TIMEOUT", "lib"]
+
+
+def _ptr(t, name, dtype=None, optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the QSA path runs only on the GPU)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def qsa_abi_version() -> int:
+    return lib().qsa_abi_version()
+
+
+def qsa_score_workspace_bytes(ntok: int, head_dim: int = 128) -> int:
+    return int(lib().qsa_score_workspace_bytes(ntok, head_dim))
+
+
+def qsa_prep(q_in, k_in, v_in, norm_w, pos0, kq, vq, ksc, vsc, q_out, q_out_f32=None,
+             eps=1e-6, rope_theta=10000.0, rope_dims=64, stream=None):
+    """Normalise + rotate q_in into q_out (fp16) / q_out_f32 and quantise k_in,
+    v_in into cache rows pos0 .. pos0+ntok-1.  Shapes: q_in [T, Hq, D] fp32,
+    k_in / v_in [T, 1, D] fp32, norm_w [D], kq / vq [C, D] int8, ksc / vsc
+    [C, D/32] fp16."""
+    import torch
+    T, H, D = q_in.shape
+    a = _abi.PrepArgs(ntok=T, pos0=int(pos0), n_q_heads=H, n_kv_heads=k_in.shape[1], head_dim=D, group=32,
+                      rope_dims=int(rope_dims), cache_cells=kq.shape[0], eps=float(eps),
+                      rope_theta=float(rope_theta),
+                      q_in=_ptr(q_in, "q_in", torch.float32), k_in=_ptr(k_in, "k_in", torch.float32),
+                      v_in=_ptr(v_in, "v_in", torch.float32), norm_w=_ptr(norm_w, "norm_w", torch.float32),
+                      q_out=_ptr(q_out, "q_out", torch.float16),
+                      q_out_f32=_ptr(q_out_f32, "q_out_f32", torch.float32, optional=True),
+                      kq=_ptr(kq, "kq", torch.int8), vq=_ptr(vq, "vq", torch.int8),
+                      ksc=_ptr(ksc, "ksc", torch.float16), vsc=_ptr(vsc, "vsc", torch.float16))
+    _abi.check(lib().qsa_prep(ctypes.byref(a), _stream(stream)))
+
+
+def qsa_score(q, kq, ksc, pos0, scores, workspace, err=None, stream=None):
+    """scores[t, c] for c <= pos0 + t (others untouched).  q [T, Hq, D] fp32 or
+    fp16; scores [T, ld] fp32 with ld >= pos0 + T; workspace a uint8 CUDA
+    tensor of at least qsa_score_workspace_bytes(T) bytes."""
+    import torch
+    T, H, D = q.shape
+    if q.dtype not in (torch.float32, torch.float16):
+        raise ValueError("q must be float32 or float16")
+    if scores.dim() != 2 or scores.shape[0] < T:
+        raise ValueError("scores must be [T, ld]")
+    a = _abi.ScoreArgs(ntok=T, pos0=int(pos0), n_q_heads=H, head_dim=D, group=32, cache_cells=kq.shape[0],
+                       q=_ptr(q, "q"), q_dtype=_abi.QSA_F16 if q.dtype == torch.float16 else _abi.QSA_F32,
+                       kq=_ptr(kq, "kq", torch.int8), ksc=_ptr(ksc, "ksc", torch.float16),
+                       scores=_ptr(scores, "scores", torch.float32), ld=scores.shape[1],
+                       workspace=_ptr(workspace, "workspace"),
+                       workspace_bytes=workspace.numel() * workspace.element_size(),
+                       err=_ptr(err, "err", torch.int32, optional=True))
+    _abi.check(lib().qsa_score(ctypes.byref(a), _stream(stream)))
+
+
+def qsa_attn(q, kq, vq, ksc, vsc, ids, out, softmax_scale=None, part=None, err=None, stream=None):
+    """Chunked attention of q [T, Hq, D] fp16 over ids [T, W] int32 (-1 =
+    padding, W a multiple of 64) into out [T, Hq, D] fp16.  part, if given,
+    is [T, W/64, Hq, D+2] fp32 and selects the split per-chunk + merge path."""
+    import torch
+    T, H, D = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    a = _abi.AttnArgs(ntok=T, n_q_heads=H, n_kv_heads=1, head_dim=D, group=32, cache_cells=kq.shape[0],
+                      width=ids.shape[1], q=_ptr(q, "q", torch.float16), kq=_ptr(kq, "kq", torch.int8),
+                      vq=_ptr(vq, "vq", torch.int8), ksc=_ptr(ksc, "ksc", torch.float16),
+                      vsc=_ptr(vsc, "vsc", torch.float16), ids=_ptr(ids, "ids", torch.int32),
+                      softmax_scale=float(softmax_scale), out=_ptr(out, "out", torch.float16),
+                      part=_ptr(part, "part", torch.float32, optional=True),
+                      err=_ptr(err, "err", torch.int32, optional=True))
+    _abi.check(lib().qsa_attn(ctypes.byref(a), _stream(stream)))

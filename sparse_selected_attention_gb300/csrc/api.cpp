@@ -1,0 +1,131 @@
+// C ABI of the QSA hot path: host-side argument validation and dispatch.
+//
+// Validation makes no CUDA call, so every argument error is reported before
+// anything touches the device (and can be exercised on a machine without a
+// GPU).  Only accepted arguments reach the launchers in the .cu files.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+#include "qsa.h"
+#include "qsa_internal.h"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+qsa_status fail(qsa_status s, const char *what) {
+    std::snprintf(g_last_error, sizeof g_last_error, "%s", what);
+    return s;
+}
+
+qsa_status cuda_fail(cudaError_t e, const char *where) {
+    std::snprintf(g_last_error, sizeof g_last_error, "%s: %s", where, cudaGetErrorString(e));
+    return QSA_ERR_CUDA;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int kHeadDim = 128;
+constexpr int kGroup = 32;
+constexpr long long kMaxPos = 1ll << 29;  // positions stay exact in the rotation angle product
+
+}  // namespace
+
+extern "C" {
+
+int qsa_abi_version(void) { return QSA_ABI_VERSION; }
+
+const char *qsa_last_error(void) { return g_last_error; }
+
+const char *qsa_status_str(qsa_status s) {
+    switch (s) {
+        case QSA_OK: return "ok";
+        case QSA_ERR_INVALID_ARG: return "invalid argument";
+        case QSA_ERR_UNSUPPORTED: return "unsupported shape";
+        case QSA_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+size_t qsa_score_workspace_bytes(int ntok, int head_dim) {
+    if (ntok < 0 || head_dim != kHeadDim) return 0;
+    const size_t pad = ((size_t)ntok + qsa::kScoreTokTile - 1) / qsa::kScoreTokTile * qsa::kScoreTokTile;
+    return pad * 2 * (size_t)head_dim * sizeof(uint16_t);
+}
+
+qsa_status qsa_prep(const qsa_prep_args *a, void *stream) {
+    g_last_error[0] = 0;
+    if (!a) return fail(QSA_ERR_INVALID_ARG, "qsa_prep: args is NULL");
+    if (a->ntok < 0 || a->pos0 < 0) return fail(QSA_ERR_INVALID_ARG, "qsa_prep: negative ntok or pos0");
+    if (a->head_dim != kHeadDim || a->group != kGroup || a->n_kv_heads != 1 || a->n_q_heads < 1 ||
+        a->n_q_heads > 30)
+        return fail(QSA_ERR_UNSUPPORTED, "qsa_prep: supported shapes are head_dim 128, group 32, 1 KV head, 1..30 query heads");
+    if (a->rope_dims < 0 || a->rope_dims > a->head_dim || a->rope_dims % 8 != 0)
+        return fail(QSA_ERR_UNSUPPORTED, "qsa_prep: rope_dims must be a multiple of 8 in [0, head_dim]");
+    if ((long long)a->pos0 + a->ntok > a->cache_cells)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_prep: pos0 + ntok exceeds cache_cells");
+    if ((long long)a->pos0 + a->ntok > kMaxPos) return fail(QSA_ERR_INVALID_ARG, "qsa_prep: positions beyond 2^29");
+    if (!(a->eps >= 0.0f) || !std::isfinite(a->eps) || !(a->rope_theta > 0.0f) || !std::isfinite(a->rope_theta))
+        return fail(QSA_ERR_INVALID_ARG, "qsa_prep: eps must be finite >= 0 and rope_theta finite > 0");
+    if (a->ntok == 0) return QSA_OK;
+    if (!a->q_in || !a->k_in || !a->v_in || !a->norm_w || !a->q_out || !a->kq || !a->vq || !a->ksc || !a->vsc)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_prep: NULL buffer");
+    if (!aligned(a->q_in, 16) || !aligned(a->k_in, 16) || !aligned(a->v_in, 16) || !aligned(a->norm_w, 16) ||
+        !aligned(a->q_out, 16) || (a->q_out_f32 && !aligned(a->q_out_f32, 16)) || !aligned(a->kq, 16) ||
+        !aligned(a->vq, 16) || !aligned(a->ksc, 8) || !aligned(a->vsc, 8))
+        return fail(QSA_ERR_INVALID_ARG, "qsa_prep: misaligned buffer");
+    qsa::PrepLaunch L{a->ntok, a->pos0, a->n_q_heads, a->rope_dims, a->eps, a->rope_theta, a->q_in, a->k_in,
+                      a->v_in, a->norm_w, a->q_out, a->q_out_f32, a->kq, a->vq, a->ksc, a->vsc};
+    cudaError_t e = qsa::launch_prep(L, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_prep");
+}
+
+qsa_status qsa_score(const qsa_score_args *a, void *stream) {
+    g_last_error[0] = 0;
+    if (!a) return fail(QSA_ERR_INVALID_ARG, "qsa_score: args is NULL");
+    if (a->ntok < 0 || a->pos0 < 0) return fail(QSA_ERR_INVALID_ARG, "qsa_score: negative ntok or pos0");
+    if (a->head_dim != kHeadDim || a->group != kGroup || a->n_q_heads < 1 || a->n_q_heads > 64)
+        return fail(QSA_ERR_UNSUPPORTED, "qsa_score: supported shapes are head_dim 128, group 32, 1..64 query heads");
+    if (a->q_dtype != QSA_F32 && a->q_dtype != QSA_F16) return fail(QSA_ERR_INVALID_ARG, "qsa_score: bad q_dtype");
+    if ((long long)a->pos0 + a->ntok > a->cache_cells)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_score: pos0 + ntok exceeds cache_cells");
+    if (a->ld < (long long)a->pos0 + a->ntok) return fail(QSA_ERR_INVALID_ARG, "qsa_score: ld < pos0 + ntok");
+    if (a->ntok == 0) return QSA_OK;
+    if (!a->q || !a->kq || !a->ksc || !a->scores || !a->workspace)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_score: NULL buffer");
+    if (a->workspace_bytes < qsa_score_workspace_bytes(a->ntok, a->head_dim))
+        return fail(QSA_ERR_INVALID_ARG, "qsa_score: workspace smaller than qsa_score_workspace_bytes()");
+    if (!aligned(a->q, 16) || !aligned(a->kq, 16) || !aligned(a->ksc, 8) || !aligned(a->scores, 4) ||
+        !aligned(a->workspace, 256))
+        return fail(QSA_ERR_INVALID_ARG, "qsa_score: misaligned buffer");
+    qsa::ScoreLaunch L{a->ntok,   a->pos0, a->n_q_heads, a->cache_cells, a->q, a->q_dtype == QSA_F16 ? 1 : 0,
+                       a->kq,     a->ksc,  a->scores,    a->ld,          static_cast<uint16_t *>(a->workspace),
+                       a->err};
+    cudaError_t e = qsa::launch_score(L, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_score");
+}
+
+qsa_status qsa_attn(const qsa_attn_args *a, void *stream) {
+    g_last_error[0] = 0;
+    if (!a) return fail(QSA_ERR_INVALID_ARG, "qsa_attn: args is NULL");
+    if (a->ntok < 0 || a->cache_cells < 1) return fail(QSA_ERR_INVALID_ARG, "qsa_attn: negative ntok or empty cache");
+    if (a->head_dim != kHeadDim || a->group != kGroup || a->n_kv_heads != 1 || a->n_q_heads < 1 ||
+        a->n_q_heads > 16)
+        return fail(QSA_ERR_UNSUPPORTED, "qsa_attn: supported shapes are head_dim 128, group 32, 1 KV head, 1..16 query heads");
+    if (a->width <= 0 || a->width % 64 != 0)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_attn: width must be a positive multiple of 64");
+    if (!std::isfinite(a->softmax_scale)) return fail(QSA_ERR_INVALID_ARG, "qsa_attn: softmax_scale not finite");
+    if (a->ntok == 0) return QSA_OK;
+    if (!a->q || !a->kq || !a->vq || !a->ksc || !a->vsc || !a->ids || !a->out)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_attn: NULL buffer");
+    if (!aligned(a->q, 16) || !aligned(a->kq, 16) || !aligned(a->vq, 16) || !aligned(a->ksc, 8) ||
+        !aligned(a->vsc, 8) || !aligned(a->ids, 4) || !aligned(a->out, 16) || (a->part && !aligned(a->part, 16)))
+        return fail(QSA_ERR_INVALID_ARG, "qsa_attn: misaligned buffer");
+    qsa::AttnLaunch L{a->ntok, a->n_q_heads, a->cache_cells, a->width, a->q,  a->kq,   a->vq, a->ksc,
+                      a->vsc,  a->ids,       a->softmax_scale, a->out, a->part, a->err};
+    cudaError_t e = qsa::launch_attn(L, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_attn");
+}
+
+}  // extern "C"

@@ -1,0 +1,411 @@
+// qsa_attn: chunked attention over per-token selected cache cells.
+//
+// "round 11 track b: qsa attention and score", section "implementation and
+// evaluator": per-token selected ids with -1 padding, 64-cell chunks (the last
+// one possibly incomplete), K row pointers and the four scale groups resolved
+// once per step, V pointers and scales once per run of cells.
+// "round 5 track b: cached residual norms and fused mtp attention", sections
+// "mtp attention" and "preflight / ownership": per-chunk maxima and
+// denominators, a max-first chunk merge, and value accumulation for all 12
+// heads together so each value is loaded once per dimension per cell.
+//
+// GB300 design.  The 12 query heads share one KV row, so a cell's K and V
+// codes are gathered once and used for every head: the head dimension is the
+// M side (padded 12 -> 16) of m16n8k16 tensor-core products, cells are N for
+// Q.K^T and the contraction for P.V.  Gathered int8 rows are loaded straight
+// from global memory into the registers that form the mma fragments (no shared
+// memory staging): a permutation of the contraction index d makes each
+// thread's part of a K row one contiguous 32-byte span and its part of a V row
+// one contiguous 16-byte span, so every gather is a coalesced 16-byte load.
+// Codes are turned into exact fp16 integers with a byte-permute bias trick and
+// scaled by their fp16 group scale in the same registers.  Padding slots are
+// never dereferenced: their scores are -inf and their values zero.
+//
+// Fused path (part == NULL): one CTA per token, NW warps; each warp walks its
+// share of 32-cell units with an online max / denominator, and the warps' states
+// are merged max-first in shared memory.  Split path (part != NULL): one warp
+// per 64-cell chunk writes that chunk's (o_c, m_c, l_c); a second kernel merges
+// the chunks max-first exactly as the definition states.
+#include <cuda_fp16.h>
+#include <math_constants.h>
+
+#include "qsa.h"
+#include "qsa_internal.h"
+
+namespace qsa {
+namespace {
+
+constexpr int D = 128;
+constexpr int G = 32;
+constexpr int UNIT = 32;   // cells per warp step
+constexpr int CHUNK = 64;  // cells per chunk of the definition
+constexpr float LN2 = 0.6931471805599453f;
+constexpr float LOG2E = 1.4426950408889634f;
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+// Bytes 0..3 of w are int8 codes already xor'ed with 0x80 (i.e. code + 128).
+// 0x64xx is the fp16 value 1024 + xx, so (byte | 0x6400) - 1152 is the code,
+// exactly.  lo = (code0, code1), hi = (code2, code3).
+__device__ __forceinline__ void codes_to_h2(uint32_t wx, __half2 &lo, __half2 &hi) {
+    const uint32_t m = 0x64646464u;
+    const __half2 bias = u2h(0x64806480u);  // 1152.0 in both halves
+    lo = __hsub2(u2h(prmt(wx, m, 0x4140)), bias);
+    hi = __hsub2(u2h(prmt(wx, m, 0x4342)), bias);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Per-warp running state of one token: rows g and g+8 of the 16-head tile.
+struct State {
+    float o[16][4];  // o[jd][0..1]: row g, d = 32r + jd (+16); o[jd][2..3]: row g+8
+    float m[2];      // running maximum, base-2 logits
+    float l[2];      // running denominator, this thread's columns only
+};
+
+__device__ __forceinline__ void state_init(State &st) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st.o[j][e] = 0.0f;
+    st.m[0] = st.m[1] = -CUDART_INF_F;
+    st.l[0] = st.l[1] = 0.0f;
+}
+
+// Q fragments of token t for the permuted contraction: slot 2r+e of k-step ks
+// holds d = 32r + 4ks + e, slot 2r+8+e holds d = 32r + 4ks + 2 + e.
+__device__ __forceinline__ void load_q(const AttnLaunch &a, int t, uint32_t (&qa)[8][4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int h = g + 8 * half;
+        uint32_t w[16];
+        if (h < a.n_q_heads) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((size_t)t * a.n_q_heads + h) * D + 32 * r);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 v = __ldg(src + i);
+                w[4 * i + 0] = v.x;
+                w[4 * i + 1] = v.y;
+                w[4 * i + 2] = v.z;
+                w[4 * i + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = 0u;
+        }
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            qa[ks][half] = w[2 * ks];
+            qa[ks][2 + half] = w[2 * ks + 1];
+        }
+    }
+}
+
+// One 32-cell unit (id slots slot0 .. slot0+31) folded into the warp's state.
+// sl2 = softmax_scale * log2(e).  Returns with `bad` set if an id was < -1 or
+// >= cache_cells.
+__device__ __forceinline__ void process_unit(const AttnLaunch &a, const int32_t *__restrict__ idrow, int slot0,
+                                             const uint32_t (&qa)[8][4], State &st, float sl2, bool &bad) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
+    int id = __ldg(idrow + slot0 + lane);
+    const bool valid = id >= 0 && id < a.cache_cells;
+    bad |= (id < -1) || (id >= a.cache_cells);
+    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+    if (vmask == 0u) return;
+    if (!valid) id = -1;
+
+    // Gather: K rows of cells 8j+g (this thread's bytes 32r..32r+31, group r)
+    // and V rows of cells 16kk + 2r + {0,1,8,9} (bytes 16g..16g+15, group g/2).
+    uint4 kd[4][2];
+    __half ks[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int c = __shfl_sync(0xffffffffu, id, 8 * j + g);
+        if (c >= 0) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.kq + (size_t)c * D + 32 * r);
+            kd[j][0] = __ldg(src);
+            kd[j][1] = __ldg(src + 1);
+            ks[j] = __ushort_as_half(__ldg(a.ksc + (size_t)c * (D / G) + r));
+        } else {
+            kd[j][0] = kd[j][1] = make_uint4(0u, 0u, 0u, 0u);
+            ks[j] = __ushort_as_half(0);
+        }
+    }
+    uint4 vd[2][4];
+    __half vs[2][4];
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = __shfl_sync(0xffffffffu, id, 16 * kk + 2 * r + (e & 1) + 8 * (e >> 1));
+            if (c >= 0) {
+                vd[kk][e] = __ldg(reinterpret_cast<const uint4 *>(a.vq + (size_t)c * D + 16 * g));
+                vs[kk][e] = __ushort_as_half(__ldg(a.vsc + (size_t)c * (D / G) + (g >> 1)));
+            } else {
+                vd[kk][e] = make_uint4(0u, 0u, 0u, 0u);
+                vs[kk][e] = __ushort_as_half(0);
+            }
+        }
+
+    // S = Q K^T for the 32 cells (4 n-tiles of 8), K dequantised in registers.
+    float s[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.0f;
+        const __half2 sc = __half2half2(ks[j]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            __half2 lo, hi;
+            codes_to_h2(word_of(kd[j][k >> 2], k & 3) ^ 0x80808080u, lo, hi);
+            mma16816(s[j], qa[k], h2u(__hmul2(lo, sc)), h2u(__hmul2(hi, sc)));
+        }
+    }
+
+    // Online softmax in base 2 over this unit's valid cells.
+    float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const bool v = (vmask >> (8 * j + 2 * r + e)) & 1u;
+            s[j][e] = v ? s[j][e] * sl2 : -CUDART_INF_F;
+            s[j][e + 2] = v ? s[j][e + 2] * sl2 : -CUDART_INF_F;
+            mx0 = fmaxf(mx0, s[j][e]);
+            mx1 = fmaxf(mx1, s[j][e + 2]);
+        }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+    const float al0 = exp2f(st.m[0] - mn0), al1 = exp2f(st.m[1] - mn1);
+    st.m[0] = mn0;
+    st.m[1] = mn1;
+    float ps0 = 0.0f, ps1 = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            s[j][e] = exp2f(s[j][e] - mn0);
+            s[j][e + 2] = exp2f(s[j][e + 2] - mn1);
+            ps0 += s[j][e];
+            ps1 += s[j][e + 2];
+        }
+    st.l[0] = st.l[0] * al0 + ps0;
+    st.l[1] = st.l[1] * al1 + ps1;
+    if (__any_sync(0xffffffffu, al0 != 1.0f || al1 != 1.0f)) {
+#pragma unroll
+        for (int jd = 0; jd < 16; ++jd) {
+            st.o[jd][0] *= al0;
+            st.o[jd][1] *= al0;
+            st.o[jd][2] *= al1;
+            st.o[jd][3] *= al1;
+        }
+    }
+
+    // O += P V: P from the S accumulators (the mma C layout is the A layout),
+    // V transposed by byte permutes and dequantised by its group scale.
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+        uint32_t pa[4];
+        pa[0] = h2u(__floats2half2_rn(s[2 * kk][0], s[2 * kk][1]));
+        pa[1] = h2u(__floats2half2_rn(s[2 * kk][2], s[2 * kk][3]));
+        pa[2] = h2u(__floats2half2_rn(s[2 * kk + 1][0], s[2 * kk + 1][1]));
+        pa[3] = h2u(__floats2half2_rn(s[2 * kk + 1][2], s[2 * kk + 1][3]));
+        const __half2 v01 = __halves2half2(vs[kk][0], vs[kk][1]);
+        const __half2 v89 = __halves2half2(vs[kk][2], vs[kk][3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t w0 = word_of(vd[kk][0], i) ^ 0x80808080u, w1 = word_of(vd[kk][1], i) ^ 0x80808080u;
+            const uint32_t w8 = word_of(vd[kk][2], i) ^ 0x80808080u, w9 = word_of(vd[kk][3], i) ^ 0x80808080u;
+            __half2 a0, a1, a2, a3, c0, c1, c2, c3;
+            codes_to_h2(prmt(w0, w1, 0x5140), a0, a1);  // d = 16g + 4i + {0, 1}
+            codes_to_h2(prmt(w0, w1, 0x7362), a2, a3);  // d = 16g + 4i + {2, 3}
+            codes_to_h2(prmt(w8, w9, 0x5140), c0, c1);
+            codes_to_h2(prmt(w8, w9, 0x7362), c2, c3);
+            mma16816(st.o[4 * i + 0], pa, h2u(__hmul2(a0, v01)), h2u(__hmul2(c0, v89)));
+            mma16816(st.o[4 * i + 1], pa, h2u(__hmul2(a1, v01)), h2u(__hmul2(c1, v89)));
+            mma16816(st.o[4 * i + 2], pa, h2u(__hmul2(a2, v01)), h2u(__hmul2(c2, v89)));
+            mma16816(st.o[4 * i + 3], pa, h2u(__hmul2(a3, v01)), h2u(__hmul2(c3, v89)));
+        }
+    }
+}
+
+__device__ __forceinline__ void quad_sum_l(State &st) {
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+        st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], o);
+        st.l[1] += __shfl_xor_sync(0xffffffffu, st.l[1], o);
+    }
+}
+
+template <int NW>
+__global__ void __launch_bounds__(NW * 32) attn_fused_kernel(AttnLaunch a) {
+    extern __shared__ float smem[];
+    float *so = smem;                       // [NW][16][D]
+    float *sm = smem + NW * 16 * D;         // [NW][16]
+    float *sl = sm + NW * 16;               // [NW][16]
+    const int t = a.ntok - 1 - (int)blockIdx.x;  // longest lists first when lists grow with t
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
+    const float sl2 = a.softmax_scale * LOG2E;
+    const int32_t *idrow = a.ids + (size_t)t * a.width;
+
+    uint32_t qa[8][4];
+    load_q(a, t, qa);
+    State st;
+    state_init(st);
+    bool bad = false;
+    const int nunits = a.width / UNIT;
+    for (int u = warp; u < nunits; u += NW) process_unit(a, idrow, u * UNIT, qa, st, sl2, bad);
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && a.err) atomicOr(a.err, QSA_DEVERR_BAD_ID);
+    quad_sum_l(st);
+
+    float *ow = so + warp * 16 * D;
+#pragma unroll
+    for (int jd = 0; jd < 16; ++jd) {
+        ow[g * D + 32 * r + jd] = st.o[jd][0];
+        ow[g * D + 32 * r + 16 + jd] = st.o[jd][1];
+        ow[(g + 8) * D + 32 * r + jd] = st.o[jd][2];
+        ow[(g + 8) * D + 32 * r + 16 + jd] = st.o[jd][3];
+    }
+    if (r == 0) {
+        sm[warp * 16 + g] = st.m[0];
+        sm[warp * 16 + g + 8] = st.m[1];
+        sl[warp * 16 + g] = st.l[0];
+        sl[warp * 16 + g + 8] = st.l[1];
+    }
+    __syncthreads();
+
+    // Max-first merge of the warps' states.
+    for (int idx = threadIdx.x; idx < a.n_q_heads * D; idx += NW * 32) {
+        const int h = idx / D, d = idx % D;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm[w * 16 + h]);
+        float res = 0.0f;
+        if (M != -CUDART_INF_F) {
+            float L = 0.0f, O = 0.0f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float mw = sm[w * 16 + h];
+                if (mw == -CUDART_INF_F) continue;
+                const float sc = exp2f(mw - M);
+                L += sc * sl[w * 16 + h];
+                O += sc * so[(w * 16 + h) * D + d];
+            }
+            res = O / L;
+        }
+        a.out[((size_t)t * a.n_q_heads + h) * D + d] = __half_as_ushort(__float2half_rn(res));
+    }
+}
+
+// Split path, part 1: one warp per (token, 64-cell chunk) writes the chunk's
+// unnormalised values, maximum (natural-log units) and denominator.
+template <int NW>
+__global__ void __launch_bounds__(NW * 32) attn_chunk_kernel(AttnLaunch a) {
+    const int t = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
+    const int nch = a.width / CHUNK;
+    const int c = blockIdx.y * NW + warp;
+    if (c >= nch) return;
+    const float sl2 = a.softmax_scale * LOG2E;
+    const int32_t *idrow = a.ids + (size_t)t * a.width;
+    uint32_t qa[8][4];
+    load_q(a, t, qa);
+    State st;
+    state_init(st);
+    bool bad = false;
+    process_unit(a, idrow, c * CHUNK, qa, st, sl2, bad);
+    process_unit(a, idrow, c * CHUNK + UNIT, qa, st, sl2, bad);
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && a.err) atomicOr(a.err, QSA_DEVERR_BAD_ID);
+    quad_sum_l(st);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int h = g + 8 * half;
+        if (h >= a.n_q_heads) continue;
+        float *dst = a.part + (((size_t)t * nch + c) * a.n_q_heads + h) * (D + 2);
+#pragma unroll
+        for (int jd = 0; jd < 16; ++jd) {
+            dst[32 * r + jd] = st.o[jd][2 * half];
+            dst[32 * r + 16 + jd] = st.o[jd][2 * half + 1];
+        }
+        if (r == 0) {
+            const float mm = st.m[half];
+            dst[D] = mm == -CUDART_INF_F ? mm : mm * LN2;
+            dst[D + 1] = st.l[half];
+        }
+    }
+}
+
+// Split path, part 2: max-first merge of the chunk partials of one token.
+__global__ void __launch_bounds__(D) attn_merge_kernel(AttnLaunch a) {
+    const int t = blockIdx.x, d = threadIdx.x;
+    const int nch = a.width / CHUNK;
+    for (int h = 0; h < a.n_q_heads; ++h) {
+        const float *base = a.part + ((size_t)t * nch * a.n_q_heads + h) * (D + 2);
+        const size_t cstride = (size_t)a.n_q_heads * (D + 2);
+        float M = -CUDART_INF_F;
+        for (int c = 0; c < nch; ++c) M = fmaxf(M, base[c * cstride + D]);
+        float res = 0.0f;
+        if (M != -CUDART_INF_F) {
+            float L = 0.0f, O = 0.0f;
+            for (int c = 0; c < nch; ++c) {
+                const float mc = base[c * cstride + D];
+                if (mc == -CUDART_INF_F) continue;
+                const float w = expf(mc - M);
+                L += w * base[c * cstride + D + 1];
+                O += w * base[c * cstride + d];
+            }
+            res = O / L;
+        }
+        a.out[((size_t)t * a.n_q_heads + h) * D + d] = __half_as_ushort(__float2half_rn(res));
+    }
+}
+
+template <int NW>
+cudaError_t launch_fused(const AttnLaunch &a, cudaStream_t s) {
+    const size_t smem = (size_t)NW * (16 * D + 32) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(attn_fused_kernel<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attn_fused_kernel<NW><<<a.ntok, NW * 32, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn(const AttnLaunch &a, cudaStream_t s) {
+    if (a.ntok == 0) return cudaSuccess;
+    if (a.part) {
+        constexpr int NW = 4;
+        const int nch = a.width / CHUNK;
+        dim3 grid(a.ntok, (nch + NW - 1) / NW);
+        attn_chunk_kernel<NW><<<grid, NW * 32, 0, s>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        attn_merge_kernel<<<a.ntok, D, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    if (a.ntok < 64) return launch_fused<8>(a, s);
+    return launch_fused<4>(a, s);
+}
+
+}  // namespace qsa

@@ -1,0 +1,127 @@
+// qsa_prep: query RMS-norm + RoPE and K/V int8 quantisation.
+//
+// "Round 36 Track C: qsa_prep Single-Barrier norm_rope & w == 128 tg_sum +
+// qsa_score_mm Loop Unrolling", section "Summary & Decision": the prep pass is
+// memory-bound on the query and K/V rows; norm_rope reduces the row's squares,
+// scales by rs and the weight g, and rotates dims below QROT with partner
+// tid ^ 32.
+//
+// One CTA per token.  Warps 0..Hq-1 own the query rows of that token, warp Hq
+// the K row and warp Hq+1 the V row.  With head_dim 128 every lane holds four
+// consecutive elements, so a row is one coalesced 512-byte load and a sum of
+// squares is five xor-shuffles.  The token's rotation angles are computed once
+// per CTA (in double, then reduced modulo 2*pi before the fp32 sincos) because
+// a single fp32 product p * inv_freq is off by up to 2e-3 rad at p ~ 32k.
+#include <cuda_fp16.h>
+
+#include "qsa_internal.h"
+
+namespace qsa {
+namespace {
+
+constexpr int D = 128;
+constexpr int G = 32;
+
+struct PrepParams {
+    PrepLaunch a;
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__global__ void __launch_bounds__(1024) prep_kernel(PrepParams P) {
+    const PrepLaunch &a = P.a;
+    const int t = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ float2 cs[D / 2];
+    const int half = a.rope_dims >> 1;
+
+    if ((int)threadIdx.x < half) {
+        const int i = threadIdx.x;
+        const float f = (float)pow((double)a.rope_theta, -2.0 * (double)i / (double)a.rope_dims);
+        const double ang = (double)(a.pos0 + t) * (double)f;  // exact: 24-bit x < 2^29
+        const double two_pi = 6.283185307179586;
+        const double k = rint(ang * (1.0 / two_pi));
+        const float r = (float)fma(-k, two_pi, ang);
+        float s, c;
+        sincosf(r, &s, &c);
+        cs[i] = make_float2(c, s);
+    }
+    __syncthreads();
+
+    if (warp < a.n_q_heads) {
+        const size_t row = ((size_t)t * a.n_q_heads + warp) * D;
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(a.q_in + row) + lane);
+        const float4 g = __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane);
+        float ss = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+        ss = warp_sum(ss);
+        const float rs = __frsqrt_rn(ss / (float)D + a.eps);
+        float y[4] = {(rs * x.x) * g.x, (rs * x.y) * g.y, (rs * x.z) * g.z, (rs * x.w) * g.w};
+        if (half > 0) {
+            const int sh = half >> 2;  // lanes between partners (half is a multiple of 4)
+            float up[4], dn[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                up[e] = __shfl_down_sync(0xffffffffu, y[e], sh);
+                dn[e] = __shfl_up_sync(0xffffffffu, y[e], sh);
+            }
+            const int i0 = lane * 4;
+            if (i0 < half) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 c = cs[i0 + e];
+                    y[e] = y[e] * c.x - up[e] * c.y;
+                }
+            } else if (i0 < 2 * half) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 c = cs[i0 - half + e];
+                    y[e] = y[e] * c.x + dn[e] * c.y;
+                }
+            }
+        }
+        const __half2 h01 = __floats2half2_rn(y[0], y[1]);
+        const __half2 h23 = __floats2half2_rn(y[2], y[3]);
+        uint2 hv;
+        hv.x = *reinterpret_cast<const uint32_t *>(&h01);
+        hv.y = *reinterpret_cast<const uint32_t *>(&h23);
+        reinterpret_cast<uint2 *>(a.q_out + row)[lane] = hv;
+        if (a.q_out_f32) reinterpret_cast<float4 *>(a.q_out_f32 + row)[lane] = make_float4(y[0], y[1], y[2], y[3]);
+    } else if (warp < a.n_q_heads + 2) {
+        const bool is_v = warp == a.n_q_heads + 1;
+        const float *src = (is_v ? a.v_in : a.k_in) + (size_t)t * D;
+        int8_t *dst = (is_v ? a.vq : a.kq) + (size_t)(a.pos0 + t) * D;
+        uint16_t *sdst = (is_v ? a.vsc : a.ksc) + (size_t)(a.pos0 + t) * (D / G);
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(src) + lane);
+        float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const __half sh = __float2half_rn(__fdiv_rn(amax, 127.0f));
+        const float sf = __half2float(sh);
+        const float xv[4] = {x.x, x.y, x.z, x.w};
+        uint32_t packed = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float c = 0.0f;
+            if (sf != 0.0f) c = fminf(fmaxf(rintf(__fdiv_rn(xv[e], sf)), -127.0f), 127.0f);
+            packed |= ((uint32_t)(uint8_t)(int8_t)(int)c) << (8 * e);
+        }
+        reinterpret_cast<uint32_t *>(dst)[lane] = packed;
+        if ((lane & 7) == 0) sdst[lane >> 3] = __half_as_ushort(sh);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const PrepLaunch &a, cudaStream_t s) {
+    if (a.ntok == 0) return cudaSuccess;
+    PrepParams P{a};
+    const int threads = 32 * (a.n_q_heads + 2);
+    prep_kernel<<<a.ntok, threads, 0, s>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace qsa

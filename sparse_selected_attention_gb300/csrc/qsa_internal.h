@@ -1,0 +1,52 @@
+// Internal launch interface between the C ABI (api.cpp) and the kernels.
+// Host-only declarations; every pointer here has already been validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace qsa {
+
+struct PrepLaunch {
+    int ntok, pos0, n_q_heads, rope_dims;
+    float eps, rope_theta;
+    const float *q_in, *k_in, *v_in, *norm_w;
+    uint16_t *q_out;
+    float *q_out_f32;
+    int8_t *kq, *vq;
+    uint16_t *ksc, *vsc;
+};
+
+struct ScoreLaunch {
+    int ntok, pos0, n_q_heads, cache_cells;
+    const void *q;
+    int q_f16;
+    const int8_t *kq;
+    const uint16_t *ksc;
+    float *scores;
+    int64_t ld;
+    uint16_t *qsum;  // workspace: [ntok_pad, 2, 128] fp16 (hi row, lo row)
+    unsigned int *err;
+};
+
+struct AttnLaunch {
+    int ntok, n_q_heads, cache_cells, width;
+    const uint16_t *q;
+    const int8_t *kq, *vq;
+    const uint16_t *ksc, *vsc;
+    const int32_t *ids;
+    float softmax_scale;
+    uint16_t *out;
+    float *part;
+    unsigned int *err;
+};
+
+// Token rows of the score workspace are padded to this multiple.
+constexpr int kScoreTokTile = 64;
+
+cudaError_t launch_prep(const PrepLaunch &a, cudaStream_t s);
+cudaError_t launch_score(const ScoreLaunch &a, cudaStream_t s);
+cudaError_t launch_attn(const AttnLaunch &a, cudaStream_t s);
+
+}  // namespace qsa

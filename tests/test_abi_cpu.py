@@ -1,0 +1,124 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, and rejects bad arguments before any CUDA call."""
+import ctypes
+
+import pytest
+
+from sparse_selected_attention_gb300 import _abi, build
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return _abi.lib()
+
+
+def test_exports_every_header_function(L):
+    names = _abi.header_functions()
+    assert {"qsa_prep", "qsa_score", "qsa_attn", "qsa_status_str", "qsa_last_error", "qsa_abi_version",
+            "qsa_score_workspace_bytes"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+    assert L.qsa_abi_version() == 1
+    assert L.qsa_status_str(0) == b"ok" and L.qsa_status_str(2) == b"unsupported shape"
+
+
+def test_workspace_bytes(L):
+    assert L.qsa_score_workspace_bytes(1, 128) == 64 * 512
+    assert L.qsa_score_workspace_bytes(1984, 128) == 1984 * 512
+    assert L.qsa_score_workspace_bytes(1985, 128) == 2048 * 512
+    assert L.qsa_score_workspace_bytes(10, 64) == 0
+
+
+FAKE = 1 << 20  # an aligned non-null address; never dereferenced (validation fails first)
+
+
+def _attn(**kw):
+    a = _abi.AttnArgs(ntok=4, n_q_heads=12, n_kv_heads=1, head_dim=128, group=32, cache_cells=100, width=128,
+                      q=FAKE, kq=FAKE, vq=FAKE, ksc=FAKE, vsc=FAKE, ids=FAKE, softmax_scale=0.088, out=FAKE,
+                      part=None, err=None)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def _status(L, fn, args):
+    s = getattr(L, fn)(ctypes.byref(args), None)
+    return s, L.qsa_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(width=100), _abi.QSA_ERR_INVALID_ARG),
+    (dict(width=0), _abi.QSA_ERR_INVALID_ARG),
+    (dict(n_q_heads=17), _abi.QSA_ERR_UNSUPPORTED),
+    (dict(head_dim=256), _abi.QSA_ERR_UNSUPPORTED),
+    (dict(n_kv_heads=2), _abi.QSA_ERR_UNSUPPORTED),
+    (dict(group=64), _abi.QSA_ERR_UNSUPPORTED),
+    (dict(ids=None), _abi.QSA_ERR_INVALID_ARG),
+    (dict(out=FAKE + 2), _abi.QSA_ERR_INVALID_ARG),
+    (dict(kq=FAKE + 8), _abi.QSA_ERR_INVALID_ARG),
+    (dict(cache_cells=0), _abi.QSA_ERR_INVALID_ARG),
+    (dict(softmax_scale=float("inf")), _abi.QSA_ERR_INVALID_ARG),
+    (dict(ntok=-1), _abi.QSA_ERR_INVALID_ARG),
+])
+def test_attn_rejects(L, kw, want):
+    s, msg = _status(L, "qsa_attn", _attn(**kw))
+    assert s == want and msg.startswith("qsa_attn")
+
+
+def test_attn_zero_tokens_is_a_no_op(L):
+    assert _status(L, "qsa_attn", _attn(ntok=0, q=None, out=None))[0] == _abi.QSA_OK
+
+
+def _score(**kw):
+    a = _abi.ScoreArgs(ntok=64, pos0=10, n_q_heads=12, head_dim=128, group=32, cache_cells=74, q=FAKE,
+                       q_dtype=_abi.QSA_F32, kq=FAKE, ksc=FAKE, scores=FAKE, ld=74, workspace=FAKE,
+                       workspace_bytes=1 << 20, err=None)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(cache_cells=73), _abi.QSA_ERR_INVALID_ARG),
+    (dict(ld=73), _abi.QSA_ERR_INVALID_ARG),
+    (dict(q_dtype=7), _abi.QSA_ERR_INVALID_ARG),
+    (dict(workspace_bytes=100), _abi.QSA_ERR_INVALID_ARG),
+    (dict(workspace=FAKE + 16), _abi.QSA_ERR_INVALID_ARG),
+    (dict(workspace=None), _abi.QSA_ERR_INVALID_ARG),
+    (dict(head_dim=64), _abi.QSA_ERR_UNSUPPORTED),
+    (dict(n_q_heads=0), _abi.QSA_ERR_UNSUPPORTED),
+    (dict(ksc=FAKE + 2), _abi.QSA_ERR_INVALID_ARG),
+])
+def test_score_rejects(L, kw, want):
+    s, msg = _status(L, "qsa_score", _score(**kw))
+    assert s == want and msg.startswith("qsa_score")
+
+
+def _prep(**kw):
+    a = _abi.PrepArgs(ntok=8, pos0=3000, n_q_heads=12, n_kv_heads=1, head_dim=128, group=32, rope_dims=64,
+                      cache_cells=3008, eps=1e-6, rope_theta=10000.0, q_in=FAKE, k_in=FAKE, v_in=FAKE,
+                      norm_w=FAKE, q_out=FAKE, q_out_f32=None, kq=FAKE, vq=FAKE, ksc=FAKE, vsc=FAKE)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(cache_cells=3007), _abi.QSA_ERR_INVALID_ARG),
+    (dict(rope_dims=60), _abi.QSA_ERR_UNSUPPORTED),
+    (dict(rope_dims=136), _abi.QSA_ERR_UNSUPPORTED),
+    (dict(n_kv_heads=2), _abi.QSA_ERR_UNSUPPORTED),
+    (dict(eps=-1.0), _abi.QSA_ERR_INVALID_ARG),
+    (dict(q_in=FAKE + 4), _abi.QSA_ERR_INVALID_ARG),
+    (dict(vsc=None), _abi.QSA_ERR_INVALID_ARG),
+    (dict(pos0=(1 << 29) - 4, cache_cells=1 << 30), _abi.QSA_ERR_INVALID_ARG),
+])
+def test_prep_rejects(L, kw, want):
+    s, msg = _status(L, "qsa_prep", _prep(**kw))
+    assert s == want and msg.startswith("qsa_prep")
+
+
+def test_null_args_pointer(L):
+    for fn in ("qsa_prep", "qsa_score", "qsa_attn"):
+        assert getattr(L, fn)(None, None) == _abi.QSA_ERR_INVALID_ARG

@@ -1,0 +1,154 @@
+"""qsa_attn on the GPU against the CPU oracle, through the C ABI.
+
+Covers the four attention workloads at full size (the decode ones and the
+short prompt one on every token, the long prompt one on a seeded sample of
+token rows that includes every edge-mode row of the sample), the width-2051
+case with a three-cell last chunk, the decode width matrix, padding-only
+tokens, out-of-range ids, the split (per-chunk + merge) path with its chunk
+partials, and other head counts.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention
+from sparse_selected_attention_gb300 import QSA_DEVERR_BAD_ID, qsa_attn
+from sparse_selected_attention_gb300 import workloads as wl
+from tests.gpu_helpers import assert_f16_close, cache_dev, dev
+
+pytestmark = pytest.mark.gpu
+
+SCALE = 1.0 / math.sqrt(128.0)
+
+
+def run_gpu(q, cache, ids, part=False, heads=None):
+    kq, vq, ksc, vsc = cache_dev(cache)
+    qd = dev(q)
+    idd = dev(ids.astype(np.int32))
+    T, H, D = q.shape
+    out = torch.full((T, H, D), float("nan"), dtype=torch.float16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pt = None
+    if part:
+        pt = torch.full((T, ids.shape[1] // 64, H, D + 2), float("nan"), dtype=torch.float32, device="cuda")
+    qsa_attn(qd, kq, vq, ksc, vsc, idd, out, SCALE, part=pt, err=err)
+    torch.cuda.synchronize()
+    return out.cpu(), (pt.cpu().numpy() if part else None), int(err.item())
+
+
+def check(q, cache, ids, rows=None, what="", part=False):
+    out, pt, err = run_gpu(q, cache, ids, part=part)
+    ref64, _, refpart, bad = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, ids, SCALE, rows=rows,
+                                       want_part=part)
+    sel = out if rows is None else out[rows]
+    assert_f16_close(sel, ref64, what)
+    assert bool(err & QSA_DEVERR_BAD_ID) == bad
+    return out, pt, refpart, rows
+
+
+@pytest.mark.parametrize("w", [wl.TINY_DECODE, wl.MTP_DECODE])
+def test_decode_workloads_full(cuda_device, w):
+    cache = wl.make_cache(w.cells, seed=w.seed)
+    q = wl.queries_f16(w.ntok, seed=w.seed)
+    check(q, cache, w.make_ids(), what=w.name)
+
+
+def test_prompt_short_full(cuda_device):
+    w = wl.PROMPT_SHORT
+    cache = wl.make_cache(w.cells, seed=w.seed)
+    q = wl.queries_f16(w.ntok, seed=w.seed)
+    check(q, cache, w.make_ids(), what=w.name)
+
+
+def _sample_rows(T, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(T, size=n, replace=False).tolist()) | {0, 1, 63, 64, T - 1}
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("edge", [0, 1, 2])
+def test_prompt_long_sampled(cuda_device, edge):
+    w = wl.PROMPT_LONG
+    cache = wl.make_cache(w.cells, seed=w.seed)
+    q = wl.queries_f16(w.ntok, seed=w.seed)
+    if edge == 1:
+        q = wl.edge_signed_zero(q)
+    elif edge == 2:
+        q, cache = wl.edge_cancellation(q, cache, seed=w.seed)
+    rows = _sample_rows(w.ntok, 96, 100 + edge)
+    out, _, _, _ = check(q, cache, w.make_ids(), rows=rows, what=f"{w.name} edge {edge}")
+    if edge == 1:
+        # q = +-0: every score is 0, so the output is the plain mean of the rows.
+        t = 7 * 11
+        ids = w.make_ids()[t]
+        v = cache.vq.astype(np.float64) * np.repeat(cache.vsc.astype(np.float64), 32, axis=1)
+        mean = v[ids[ids >= 0]].mean(axis=0)
+        assert_f16_close(out[t], np.broadcast_to(mean, (12, 128)), "signed-zero mean")
+
+
+def test_width_2051_three_cell_last_chunk(cuda_device):
+    cache = wl.make_cache(31990, seed=3)
+    q = wl.queries_f16(40, seed=3)
+    ids = wl.even_ids(40, 31900, width=2112, select=2051)
+    check(q, cache, ids, what="W=2112, 2051 valid")
+
+
+@pytest.mark.parametrize("n", [1, 31, 64, 65, 128, 319, 320, 321, 383, 384])
+def test_decode_width_matrix_noncontiguous(cuda_device, n):
+    cache = wl.make_cache(9000, seed=20)
+    q = wl.queries_f16(2, seed=20 + n)
+    rng = np.random.default_rng(n)
+    ids = np.full((2, 384), -1, dtype=np.int32)
+    for t in range(2):
+        ids[t, :n] = np.sort(rng.choice(9000, size=n, replace=False))
+    check(q, cache, ids, what=f"width {n}")
+
+
+def test_padding_only_tokens_and_bad_ids(cuda_device):
+    cache = wl.make_cache(500, seed=21)
+    q = wl.queries_f16(5, seed=21)
+    ids = np.full((5, 256), -1, dtype=np.int32)
+    ids[1, 100:180] = np.arange(80)
+    ids[3, 5] = 500           # == cache_cells: out of range
+    ids[3, 6] = -2            # below -1
+    ids[3, 7] = 17
+    ids[4, 200] = 499
+    out, _, _, _ = check(q, cache, ids, what="padding / bad ids")
+    for t in (0, 2):
+        o = out[t].numpy()
+        assert np.all(o == 0) and not np.signbit(o).any()
+
+
+def test_split_path_partials_and_merge(cuda_device):
+    cache = wl.make_cache(5000, seed=22)
+    q = wl.queries_f16(33, seed=22)
+    ids = wl.even_ids(33, 4960, width=448, select=400)
+    ids[5, 64:128] = -1                       # an empty chunk in the middle
+    out, pt, refpart, _ = check(q, cache, ids, what="split path", part=True)
+    D = 128
+    # chunk partials: m and l compared through exp(m) l scale, o relative to l * max|v|.
+    ref_m, ref_l, ref_o = refpart[..., D], refpart[..., D + 1], refpart[..., :D]
+    g_m, g_l, g_o = pt[..., D], pt[..., D + 1], pt[..., :D]
+    empty = ~np.isfinite(ref_m)
+    assert np.array_equal(np.isfinite(g_m), ~empty)
+    assert np.all(g_l[empty] == 0) and np.all(g_o[empty] == 0)
+    ne = ~empty
+    np.testing.assert_allclose(g_m[ne], ref_m[ne], atol=2e-3, rtol=2e-3)
+    np.testing.assert_allclose(g_l[ne] * np.exp(g_m[ne] - ref_m[ne]), ref_l[ne], rtol=2e-3)
+    vmax = 127 * 0.0201
+    scale = (ref_l * vmax)[..., None]
+    err = np.abs(g_o * np.exp(g_m - np.where(ne, ref_m, 0))[..., None] - ref_o)
+    assert np.all(err[ne] <= 2e-3 * scale[ne] + 1e-6)
+    # fused and split paths agree to the fp16 tolerance
+    out2, _, _ = run_gpu(q, cache, ids, part=False)
+    assert_f16_close(out2, out.float().numpy().astype(np.float64), "fused vs split")
+
+
+@pytest.mark.parametrize("heads", [1, 8, 16])
+def test_other_head_counts(cuda_device, heads):
+    cache = wl.make_cache(3000, seed=23)
+    q = wl.queries_f16(70, seed=23, heads=heads)
+    ids = wl.even_ids(70, 2900, width=1024, select=1000)
+    check(q, cache, ids, what=f"{heads} heads")

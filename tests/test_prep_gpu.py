@@ -1,0 +1,72 @@
+"""qsa_prep on the GPU against the CPU oracle, through the C ABI.
+
+Shapes follow the prep measurements on the pages (P = 0 / 3000, nt = 1, 2, 4,
+8, 1984, 2048) plus long-context positions.  Quantised codes and scale bits
+must match bit for bit; cache rows outside pos0 .. pos0+T-1 must be untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import prep as oracle_prep
+from sparse_selected_attention_gb300 import qsa_prep
+from sparse_selected_attention_gb300 import workloads as wl
+from tests.gpu_helpers import assert_f16_close, dev
+
+pytestmark = pytest.mark.gpu
+
+Q32_ATOL = 2e-5   # fp32 arithmetic on O(1) values: a few ulp of the row scale
+
+
+def run_case(T, pos0, rope_dims=64, heads=12, extra=7, seed=41):
+    inp = wl.prep_inputs(T, seed=seed, heads=heads)
+    C = pos0 + T + extra
+    cache = wl.make_cache(C, seed=seed)
+    kq, vq, ksc, vsc = dev(cache.kq), dev(cache.vq), dev(cache.ksc), dev(cache.vsc)
+    q_out = torch.full((T, heads, 128), float("nan"), dtype=torch.float16, device="cuda")
+    q32 = torch.full((T, heads, 128), float("nan"), dtype=torch.float32, device="cuda")
+    qsa_prep(dev(inp.q_in), dev(inp.k_in), dev(inp.v_in), dev(inp.norm_w), pos0, kq, vq, ksc, vsc, q_out,
+             q_out_f32=q32, rope_dims=rope_dims)
+    torch.cuda.synchronize()
+    ref_cache = cache.copy()
+    q64, _, _ = oracle_prep(inp.q_in, inp.k_in, inp.v_in, inp.norm_w, pos0, ref_cache.kq, ref_cache.vq,
+                            ref_cache.ksc, ref_cache.vsc, rope_dims=rope_dims)
+    assert_f16_close(q_out.cpu(), q64, f"q fp16 T={T} pos0={pos0}")
+    np.testing.assert_allclose(q32.cpu().numpy(), q64, atol=Q32_ATOL, rtol=0)
+    for name, g, r in (("kq", kq, ref_cache.kq), ("vq", vq, ref_cache.vq),
+                       ("ksc", ksc, ref_cache.ksc.view(np.int16)), ("vsc", vsc, ref_cache.vsc.view(np.int16))):
+        gn = g.cpu().numpy()
+        if gn.dtype == np.float16:
+            gn = gn.view(np.int16)
+        assert np.array_equal(gn, r), f"{name} differs from the oracle (T={T}, pos0={pos0})"
+
+
+@pytest.mark.parametrize("T,pos0", [(1, 3000), (2, 3000), (4, 3000), (8, 3000), (1984, 0), (1984, 3000),
+                                    (2048, 3000), (37, 30000), (5, 31979)])
+def test_prep_shapes(cuda_device, T, pos0):
+    run_case(T, pos0)
+
+
+@pytest.mark.parametrize("rope_dims", [0, 8, 128])
+def test_prep_rope_dims(cuda_device, rope_dims):
+    run_case(19, 1234, rope_dims=rope_dims)
+
+
+def test_prep_zero_group_and_large_values(cuda_device):
+    T, pos0 = 3, 10
+    inp = wl.prep_inputs(T, seed=42)
+    inp.k_in[0, 0, 32:64] = 0.0            # a zero group -> scale 0, codes 0
+    inp.v_in[1, 0, :] *= 1e4               # large magnitudes
+    inp.v_in[2, 0, 96:] = 1e-30            # tiny group -> fp16 scale underflows to 0
+    C = pos0 + T
+    cache = wl.make_cache(C, seed=42)
+    kq, vq, ksc, vsc = dev(cache.kq), dev(cache.vq), dev(cache.ksc), dev(cache.vsc)
+    q_out = torch.empty((T, 12, 128), dtype=torch.float16, device="cuda")
+    qsa_prep(dev(inp.q_in), dev(inp.k_in), dev(inp.v_in), dev(inp.norm_w), pos0, kq, vq, ksc, vsc, q_out)
+    torch.cuda.synchronize()
+    ref = cache.copy()
+    oracle_prep(inp.q_in, inp.k_in, inp.v_in, inp.norm_w, pos0, ref.kq, ref.vq, ref.ksc, ref.vsc)
+    assert np.array_equal(kq.cpu().numpy(), ref.kq) and np.array_equal(vq.cpu().numpy(), ref.vq)
+    assert np.array_equal(ksc.cpu().numpy().view(np.int16), ref.ksc.view(np.int16))
+    assert np.array_equal(vsc.cpu().numpy().view(np.int16), ref.vsc.view(np.int16))
+    assert float(ref.ksc[pos0, 1]) == 0.0 and float(ref.vsc[pos0 + 2, 3]) == 0.0

@@ -1,0 +1,68 @@
+"""qsa_score on the GPU against the CPU oracle, through the C ABI.
+
+Small shapes are compared on every causal cell; the four full-size positions
+(T = 1984 at pos0 0 / 2048 / 8192 / 30000) on a seeded sample of token rows
+that includes tile boundaries.  Every non-causal element of the output must
+still hold the caller's sentinel bit pattern, over the whole buffer.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import score, score_abs_bound
+from sparse_selected_attention_gb300 import qsa_score, qsa_score_workspace_bytes
+from sparse_selected_attention_gb300 import workloads as wl
+from tests.gpu_helpers import SENTINEL_BITS, assert_score_close, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(q, cache, pos0, ld=None, dtype=np.float32):
+    T = q.shape[0]
+    C = cache.cells
+    ld = ld or pos0 + T
+    qd = dev(q.astype(dtype))
+    kq, ksc = dev(cache.kq), dev(cache.ksc)
+    scores = torch.full((T, ld), 0, dtype=torch.int32, device="cuda").fill_(SENTINEL_BITS).view(torch.float32)
+    ws = torch.empty(qsa_score_workspace_bytes(T), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qsa_score(qd, kq, ksc, pos0, scores, ws, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    # Untouched cells keep the sentinel: checked on the device over the whole buffer.
+    causal = torch.arange(ld, device="cuda")[None, :] <= (pos0 + torch.arange(T, device="cuda"))[:, None]
+    bits = scores.view(torch.int32)
+    assert bool(torch.all(bits[~causal] == SENTINEL_BITS))
+    assert not bool(torch.any(bits[causal] == SENTINEL_BITS))
+    return scores
+
+
+def _compare(q, cache, pos0, scores, rows, what, q_used=None):
+    qq = q if q_used is None else q_used
+    ref = score(qq, cache.kq, cache.ksc, pos0, rows=rows)
+    A = score_abs_bound(qq, cache.kq, cache.ksc, pos0, rows=rows)
+    g = scores[torch.as_tensor(rows, device="cuda")].cpu().numpy()[:, : ref.shape[1]]
+    return assert_score_close(g, ref, A, what)
+
+
+@pytest.mark.parametrize("T,pos0", [(1, 0), (5, 0), (70, 0), (200, 100), (130, 2050), (64, 2052), (129, 127)])
+@pytest.mark.parametrize("dtype", [np.float32, np.float16])
+def test_small_all_cells(cuda_device, T, pos0, dtype):
+    cache = wl.make_cache(pos0 + T, seed=31)
+    cache.ksc[3] = 0            # a dead key: scores exactly 0
+    q = wl.queries_f32(T, seed=31)
+    scores = run_gpu(q, cache, pos0, ld=pos0 + T + 5, dtype=dtype)
+    q_used = q.astype(dtype)
+    _compare(q, cache, pos0, scores, np.arange(T), f"T={T} pos0={pos0} {dtype.__name__}", q_used)
+    assert torch.all(scores[:, 3] == 0)
+
+
+@pytest.mark.parametrize("pos0", wl.SCORE_POS0)
+def test_full_size_sampled_rows(cuda_device, pos0):
+    T = wl.SCORE_NTOK
+    cache = wl.make_cache(pos0 + T, seed=5)
+    q = wl.queries_f32(T, seed=5)
+    scores = run_gpu(q, cache, pos0)
+    rng = np.random.default_rng(pos0)
+    rows = np.array(sorted(set(rng.choice(T, 24, replace=False).tolist()) | {0, 63, 64, 127, 1983}))
+    _compare(q, cache, pos0, scores, rows, f"T=1984 pos0={pos0}")

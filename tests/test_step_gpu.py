@@ -1,0 +1,43 @@
+"""The whole hot path in sequence on the GPU (prep -> score -> attention) against
+the same sequence in the oracle, on a small long-context case."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention, prep as oracle_prep, score, score_abs_bound
+from sparse_selected_attention_gb300 import qsa_attn, qsa_prep, qsa_score, qsa_score_workspace_bytes
+from sparse_selected_attention_gb300 import workloads as wl
+from tests.gpu_helpers import assert_f16_close, assert_score_close, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def test_prep_score_attn_pipeline(cuda_device):
+    T, pos0 = 150, 4000
+    C = pos0 + T
+    inp = wl.prep_inputs(T, seed=51)
+    cache = wl.make_cache(C, seed=51)
+    ids = wl.even_ids(T, pos0, width=2048)
+    kq, vq, ksc, vsc = dev(cache.kq), dev(cache.vq), dev(cache.ksc), dev(cache.vsc)
+    q16 = torch.empty((T, 12, 128), dtype=torch.float16, device="cuda")
+    q32 = torch.empty((T, 12, 128), dtype=torch.float32, device="cuda")
+    qsa_prep(dev(inp.q_in), dev(inp.k_in), dev(inp.v_in), dev(inp.norm_w), pos0, kq, vq, ksc, vsc, q16,
+             q_out_f32=q32)
+    scores = torch.full((T, C), float("nan"), device="cuda")
+    ws = torch.empty(qsa_score_workspace_bytes(T), dtype=torch.uint8, device="cuda")
+    qsa_score(q32, kq, ksc, pos0, scores, ws)
+    out = torch.empty((T, 12, 128), dtype=torch.float16, device="cuda")
+    qsa_attn(q16, kq, vq, ksc, vsc, dev(ids), out)
+    torch.cuda.synchronize()
+
+    ref = cache.copy()
+    q64, _, _ = oracle_prep(inp.q_in, inp.k_in, inp.v_in, inp.norm_w, pos0, ref.kq, ref.vq, ref.ksc, ref.vsc)
+    assert np.array_equal(kq.cpu().numpy(), ref.kq) and np.array_equal(vq.cpu().numpy(), ref.vq)
+    # The oracle's score and attention consume the oracle's own prep output.
+    S = score(q64, ref.kq, ref.ksc, pos0)
+    A = score_abs_bound(q64, ref.kq, ref.ksc, pos0)
+    assert_score_close(scores.cpu().numpy(), S, A, "pipeline scores")
+    o64, _, _, _ = attention(q64.astype(np.float16), ref.kq, ref.vq, ref.ksc, ref.vsc, ids, 1 / math.sqrt(128))
+    assert_f16_close(out.cpu(), o64, "pipeline attention")
