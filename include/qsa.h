@@ -160,6 +160,33 @@ typedef struct {
     unsigned int *err;
 } qsa_attn_args;
 
+/*
+ * qsa_score_noalloc -- the pages have no counterpart to this entry point; it
+ * exists for callers that cannot allocate device memory at the time they
+ * score: for instance a plugin whose host engine owns all device memory and
+ * forbids allocation inside its execute callback, or a serving loop that must
+ * not call cudaMalloc because that call can synchronise the device and has no
+ * latency bound.  It computes exactly what qsa_score computes, but instead of
+ * the caller's workspace it uses a scratch array built into the library
+ * (QSA_SCORE_NOALLOC_MAX_TOKENS * 512 bytes = 4 MiB of device memory, held on
+ * every GPU that loads the library until the process exits).  The
+ * `workspace` and `workspace_bytes` fields are ignored.
+ *
+ *  - ntok above QSA_SCORE_NOALLOC_MAX_TOKENS is rejected with
+ *    QSA_ERR_INVALID_ARG; nothing is enqueued.
+ *  - It never allocates: no cudaMalloc, cudaFree or allocating library call.
+ *  - The first call on each device looks up the scratch array's device
+ *    address (cudaGetSymbolAddress) with that device current; make that
+ *    first call before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents.
+ *    Every call rewrites what it reads, so nothing needs clearing, but two
+ *    calls whose kernels overlap on the GPU (different streams without an
+ *    ordering dependency, or different host threads) race on it and give
+ *    wrong scores: order them on one stream or with events.
+ */
+#define QSA_SCORE_NOALLOC_MAX_TOKENS 8192
+qsa_status qsa_score_noalloc(const qsa_score_args *args, void *stream);
+
 qsa_status qsa_prep(const qsa_prep_args *args, void *stream);
 qsa_status qsa_score(const qsa_score_args *args, void *stream);
 qsa_status qsa_attn(const qsa_attn_args *args, void *stream);

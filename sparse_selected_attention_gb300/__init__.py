@@ -17,7 +17,7 @@ import math
 from . import _abi
 from ._abi import (QSA_DEVERR_BAD_ID, QSA_DEVERR_TIMEOUT, QSAError, lib)  # noqa: F401
 
-__all__ = ["qsa_prep", "qsa_score", "qsa_attn", "qsa_score_workspace_bytes", "qsa_abi_version",
+__all__ = ["qsa_prep", "qsa_score", "qsa_score_noalloc", "qsa_attn", "qsa_score_workspace_bytes", "qsa_abi_version",
            "QSAError", "QSA_DEVERR_BAD_ID", "QSA_DEVERR_TIMEOUT", "lib"]
 
 
@@ -87,6 +87,24 @@ def qsa_score(q, kq, ksc, pos0, scores, workspace, err=None, stream=None):
                        workspace_bytes=workspace.numel() * workspace.element_size(),
                        err=_ptr(err, "err", torch.int32, optional=True))
     _abi.check(lib().qsa_score(ctypes.byref(a), _stream(stream)))
+
+
+def qsa_score_noalloc(q, kq, ksc, pos0, scores, err=None, stream=None):
+    """qsa_score without a caller workspace, for callers that cannot allocate
+    device memory when they score.  It uses the library's built-in scratch
+    (at most 8192 tokens), so calls must not overlap on the GPU."""
+    import torch
+    T, H, D = q.shape
+    if q.dtype not in (torch.float32, torch.float16):
+        raise ValueError("q must be float32 or float16")
+    if scores.dim() != 2 or scores.shape[0] < T:
+        raise ValueError("scores must be [T, ld]")
+    a = _abi.ScoreArgs(ntok=T, pos0=int(pos0), n_q_heads=H, head_dim=D, group=32, cache_cells=kq.shape[0],
+                       q=_ptr(q, "q"), q_dtype=_abi.QSA_F16 if q.dtype == torch.float16 else _abi.QSA_F32,
+                       kq=_ptr(kq, "kq", torch.int8), ksc=_ptr(ksc, "ksc", torch.float16),
+                       scores=_ptr(scores, "scores", torch.float32), ld=scores.shape[1],
+                       workspace=None, workspace_bytes=0, err=_ptr(err, "err", torch.int32, optional=True))
+    _abi.check(lib().qsa_score_noalloc(ctypes.byref(a), _stream(stream)))
 
 
 def qsa_attn(q, kq, vq, ksc, vsc, ids, out, softmax_scale=None, part=None, err=None, stream=None):

@@ -16,6 +16,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "qsa.h")
 QSA_OK, QSA_ERR_INVALID_ARG, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3
 QSA_DEVERR_BAD_ID, QSA_DEVERR_TIMEOUT = 1, 2
 QSA_F32, QSA_F16 = 0, 1
+QSA_SCORE_NOALLOC_MAX_TOKENS = 8192
 
 _c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
 
@@ -60,7 +61,8 @@ def lib() -> ctypes.CDLL:
                 f"{LIB_PATH} is missing: build it with `python -m sparse_selected_attention_gb300.build` "
                 "(the QSA path has no fallback)")
         L = ctypes.CDLL(LIB_PATH)
-        for name, argt in (("qsa_prep", PrepArgs), ("qsa_score", ScoreArgs), ("qsa_attn", AttnArgs)):
+        for name, argt in (("qsa_prep", PrepArgs), ("qsa_score", ScoreArgs), ("qsa_attn", AttnArgs),
+                           ("qsa_score_noalloc", ScoreArgs)):
             f = getattr(L, name)
             f.argtypes = [ctypes.POINTER(argt), _vp]
             f.restype = _c_int

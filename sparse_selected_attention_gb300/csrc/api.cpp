@@ -128,4 +128,32 @@ qsa_status qsa_attn(const qsa_attn_args *a, void *stream) {
     return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_attn");
 }
 
+// Allocation-free scoring: same checks as qsa_score minus the workspace, plus
+// the built-in scratch limit.
+qsa_status qsa_score_noalloc(const qsa_score_args *a, void *stream) {
+    g_last_error[0] = 0;
+    if (!a) return fail(QSA_ERR_INVALID_ARG, "qsa_score_noalloc: args is NULL");
+    if (a->ntok < 0 || a->pos0 < 0) return fail(QSA_ERR_INVALID_ARG, "qsa_score_noalloc: negative ntok or pos0");
+    if (a->ntok > QSA_SCORE_NOALLOC_MAX_TOKENS)
+        return fail(QSA_ERR_INVALID_ARG,
+                    "qsa_score_noalloc: ntok exceeds the built-in scratch limit (QSA_SCORE_NOALLOC_MAX_TOKENS = 8192); "
+                    "use qsa_score with a workspace");
+    if (a->head_dim != kHeadDim || a->group != kGroup || a->n_q_heads < 1 || a->n_q_heads > 64)
+        return fail(QSA_ERR_UNSUPPORTED,
+                    "qsa_score_noalloc: supported shapes are head_dim 128, group 32, 1..64 query heads");
+    if (a->q_dtype != QSA_F32 && a->q_dtype != QSA_F16)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_score_noalloc: bad q_dtype");
+    if ((long long)a->pos0 + a->ntok > a->cache_cells)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_score_noalloc: pos0 + ntok exceeds cache_cells");
+    if (a->ld < (long long)a->pos0 + a->ntok) return fail(QSA_ERR_INVALID_ARG, "qsa_score_noalloc: ld < pos0 + ntok");
+    if (a->ntok == 0) return QSA_OK;
+    if (!a->q || !a->kq || !a->ksc || !a->scores) return fail(QSA_ERR_INVALID_ARG, "qsa_score_noalloc: NULL buffer");
+    if (!aligned(a->q, 16) || !aligned(a->kq, 16) || !aligned(a->ksc, 8) || !aligned(a->scores, 4))
+        return fail(QSA_ERR_INVALID_ARG, "qsa_score_noalloc: misaligned buffer");
+    qsa::ScoreLaunch L{a->ntok, a->pos0, a->n_q_heads, a->cache_cells, a->q, a->q_dtype == QSA_F16 ? 1 : 0,
+                       a->kq,   a->ksc,  a->scores,    a->ld,          nullptr, a->err};
+    cudaError_t e = qsa::launch_score_noalloc(L, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_score_noalloc");
+}
+
 }  // extern "C"

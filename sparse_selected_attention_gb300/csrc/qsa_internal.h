@@ -47,6 +47,9 @@ constexpr int kScoreTokTile = 64;
 
 cudaError_t launch_prep(const PrepLaunch &a, cudaStream_t s);
 cudaError_t launch_score(const ScoreLaunch &a, cudaStream_t s);
+// Same launch with the library's static scratch array as the workspace;
+// a.qsum is ignored.  At most QSA_SCORE_NOALLOC_MAX_TOKENS tokens.
+cudaError_t launch_score_noalloc(const ScoreLaunch &a, cudaStream_t s);
 cudaError_t launch_attn(const AttnLaunch &a, cudaStream_t s);
 
 }  // namespace qsa

@@ -31,6 +31,8 @@
 // tensor memory and returns.
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "qsa.h"
 #include "qsa_internal.h"
 
@@ -388,6 +390,49 @@ cudaError_t launch_score(const ScoreLaunch &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     score_kernel<<<grid, THREADS, SMEM_ALLOC, s>>>(a);
     return cudaGetLastError();
+}
+
+// --- allocation-free variant --------------------------------------------------
+//
+// For callers that may not allocate device memory when they score (an engine
+// that owns all device memory, a loop that must not hit cudaMalloc's device
+// synchronisation), the q-bar workspace can instead live in this fixed array,
+// which the CUDA module reserves on each device that loads the library and
+// keeps until the process exits.  Host code must not pass the symbol itself to
+// a kernel (on the host it names a stand-in, not device memory): the device
+// address is looked up once per device with that device current.  Calls share
+// the array, so calls whose kernels overlap on the GPU race on it.
+namespace {
+
+constexpr size_t kNoAllocElems = (size_t)QSA_SCORE_NOALLOC_MAX_TOKENS * 2 * D;  // fp16 hi/lo rows
+static __device__ __align__(256) uint16_t g_noalloc_qsum[kNoAllocElems];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kMaxDevices] = {};
+
+}  // namespace
+
+cudaError_t launch_score_noalloc(const ScoreLaunch &a, cudaStream_t s) {
+    if (a.ntok == 0) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_addr[dev]) {
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_noalloc_qsum);
+            if (e != cudaSuccess) return e;
+            g_noalloc_addr[dev] = p;
+        }
+        scratch = g_noalloc_addr[dev];
+    }
+    ScoreLaunch b = a;
+    b.qsum = static_cast<uint16_t *>(scratch);
+    return launch_score(b, s);
 }
 
 }  // namespace qsa
