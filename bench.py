@@ -46,6 +46,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--ntok", type=int, default=NTOK, help="fewer tokens: for small profiling captures only")
+    p.add_argument("--pos0", type=int, default=POS0, help="another context length: for profiling captures only")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-sample-seconds", type=float, default=15.0)
@@ -221,7 +222,7 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    T, pos0 = args.ntok, POS0
+    T, pos0 = args.ntok, args.pos0
     C = pos0 + T
     inp = wl.prep_inputs(T, seed=5 + rank)
     cache = wl.make_cache(C, seed=5 + rank)
@@ -348,7 +349,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    config = {"workload": WORKLOAD, "ntok": args.ntok, "pos0": POS0, "cache_cells": POS0 + args.ntok,
+    config = {"workload": WORKLOAD, "ntok": args.ntok, "pos0": args.pos0, "cache_cells": args.pos0 + args.ntok,
               "width": WIDTH, "heads": "12 query / 1 KV", "head_dim": D,
               "l2": "flushed between steps (256 MiB write), flush outside the step events",
               "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}

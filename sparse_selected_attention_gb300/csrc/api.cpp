@@ -75,8 +75,23 @@ qsa_status qsa_prep(const qsa_prep_args *a, void *stream) {
         !aligned(a->q_out, 16) || (a->q_out_f32 && !aligned(a->q_out_f32, 16)) || !aligned(a->kq, 16) ||
         !aligned(a->vq, 16) || !aligned(a->ksc, 8) || !aligned(a->vsc, 8))
         return fail(QSA_ERR_INVALID_ARG, "qsa_prep: misaligned buffer");
-    qsa::PrepLaunch L{a->ntok, a->pos0, a->n_q_heads, a->rope_dims, a->eps, a->rope_theta, a->q_in, a->k_in,
-                      a->v_in, a->norm_w, a->q_out, a->q_out_f32, a->kq, a->vq, a->ksc, a->vsc};
+    qsa::PrepLaunch L{};
+    L.ntok = a->ntok;
+    L.pos0 = a->pos0;
+    L.n_q_heads = a->n_q_heads;
+    L.rope_dims = a->rope_dims;
+    L.eps = a->eps;
+    L.rope_theta = a->rope_theta;
+    L.q_in = a->q_in;
+    L.k_in = a->k_in;
+    L.v_in = a->v_in;
+    L.norm_w = a->norm_w;
+    L.q_out = a->q_out;
+    L.q_out_f32 = a->q_out_f32;
+    L.kq = a->kq;
+    L.vq = a->vq;
+    L.ksc = a->ksc;
+    L.vsc = a->vsc;
     cudaError_t e = qsa::launch_prep(L, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_prep");
 }

@@ -119,13 +119,53 @@ __device__ __forceinline__ void load_q(const AttnLaunch &a, int t, uint32_t (&qa
     }
 }
 
-// One 32-cell unit (id slots slot0 .. slot0+31) folded into the warp's state.
-// sl2 = softmax_scale * log2(e).  Returns with `bad` set if an id was < -1 or
-// >= cache_cells.
-__device__ __forceinline__ void process_unit(const AttnLaunch &a, const int32_t *__restrict__ idrow, int slot0,
-                                             const uint32_t (&qa)[8][4], State &st, float sl2, bool &bad) {
+// Q fragments held in registers for the whole token.
+struct QRegs {
+    uint32_t qa[8][4];
+    __device__ __forceinline__ void get(int k, uint32_t (&f)[4]) const {
+        f[0] = qa[k][0];
+        f[1] = qa[k][1];
+        f[2] = qa[k][2];
+        f[3] = qa[k][3];
+    }
+};
+
+// Q fragments read from shared memory, stored in fragment order: row h,
+// k-step k, quad lane r -> 8 bytes at h * QROW + (4k + r) * 8.  The 288-byte
+// row pitch keeps a half-warp's 8-byte reads on distinct banks.
+constexpr int QROW = 288;
+struct QSmem {
+    const uint8_t *base;  // this thread's row g
+    __device__ __forceinline__ void get(int k, uint32_t (&f)[4]) const {
+        const int r = threadIdx.x & 3;
+        const uint2 lo = *reinterpret_cast<const uint2 *>(base + (4 * k + r) * 8);
+        const uint2 hi = *reinterpret_cast<const uint2 *>(base + 8 * QROW + (4 * k + r) * 8);
+        f[0] = lo.x;
+        f[1] = hi.x;
+        f[2] = lo.y;
+        f[3] = hi.y;
+    }
+};
+
+// Stage token t's Q rows (all 16 head rows, zeros past n_q_heads) in shared
+// memory in fragment order.  Called by every thread of the CTA.
+__device__ __forceinline__ void stage_q(const AttnLaunch &a, int t, uint8_t *sq, int nthreads) {
+    for (int i = threadIdx.x; i < 16 * 32; i += nthreads) {
+        const int h = i >> 5, k = (i >> 2) & 7, r = i & 3;
+        uint2 v = make_uint2(0u, 0u);
+        if (h < a.n_q_heads)
+            v = __ldg(reinterpret_cast<const uint2 *>(a.q + ((size_t)t * a.n_q_heads + h) * D + 32 * r + 4 * k));
+        *reinterpret_cast<uint2 *>(sq + h * QROW + (4 * k + r) * 8) = v;
+    }
+}
+
+// One 32-cell unit (id slots slot0 .. slot0+31, lane's id already loaded)
+// folded into the warp's state.  sl2 = softmax_scale * log2(e).  Sets `bad`
+// if an id was < -1 or >= cache_cells.
+template <class Q>
+__device__ __forceinline__ void process_unit(const AttnLaunch &a, int id, const Q &qsrc, State &st, float sl2,
+                                             bool &bad) {
     const int lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
-    int id = __ldg(idrow + slot0 + lane);
     const bool valid = id >= 0 && id < a.cache_cells;
     bad |= (id < -1) || (id >= a.cache_cells);
     const unsigned vmask = __ballot_sync(0xffffffffu, valid);
@@ -170,12 +210,17 @@ __device__ __forceinline__ void process_unit(const AttnLaunch &a, const int32_t 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.0f;
-        const __half2 sc = __half2half2(ks[j]);
+    }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < 8; ++k) {
+        uint32_t qf[4];
+        qsrc.get(k, qf);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
             __half2 lo, hi;
+            const __half2 sc = __half2half2(ks[j]);
             codes_to_h2(word_of(kd[j][k >> 2], k & 3) ^ 0x80808080u, lo, hi);
-            mma16816(s[j], qa[k], h2u(__hmul2(lo, sc)), h2u(__hmul2(hi, sc)));
+            mma16816(s[j], qf, h2u(__hmul2(lo, sc)), h2u(__hmul2(hi, sc)));
         }
     }
 
@@ -258,8 +303,15 @@ __device__ __forceinline__ void quad_sum_l(State &st) {
     }
 }
 
+#ifndef QSA_ATTN_MINB
+#define QSA_ATTN_MINB 3
+#endif
+#ifndef QSA_ATTN_QSMEM
+#define QSA_ATTN_QSMEM 0
+#endif
+
 template <int NW>
-__global__ void __launch_bounds__(NW * 32) attn_fused_kernel(AttnLaunch a) {
+__global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_fused_kernel(AttnLaunch a) {
     extern __shared__ float smem[];
     float *so = smem;                       // [NW][16][D]
     float *sm = smem + NW * 16 * D;         // [NW][16]
@@ -268,14 +320,28 @@ __global__ void __launch_bounds__(NW * 32) attn_fused_kernel(AttnLaunch a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
     const float sl2 = a.softmax_scale * LOG2E;
     const int32_t *idrow = a.ids + (size_t)t * a.width;
+    const int nunits = a.width / UNIT;
 
-    uint32_t qa[8][4];
-    load_q(a, t, qa);
+#if QSA_ATTN_QSMEM
+    uint8_t *sq = reinterpret_cast<uint8_t *>(sl + NW * 16);
+    stage_q(a, t, sq, NW * 32);
+    __syncthreads();
+    const QSmem qsrc{sq + g * QROW};
+#else
+    QRegs qsrc;
+    load_q(a, t, qsrc.qa);
+#endif
     State st;
     state_init(st);
     bool bad = false;
-    const int nunits = a.width / UNIT;
-    for (int u = warp; u < nunits; u += NW) process_unit(a, idrow, u * UNIT, qa, st, sl2, bad);
+    // The next unit's id is loaded one unit ahead, so each unit's critical
+    // path holds one dependent global load (the row gather), not two.
+    int id_next = warp < nunits ? __ldg(idrow + warp * UNIT + lane) : -1;
+    for (int u = warp; u < nunits; u += NW) {
+        const int id = id_next;
+        if (u + NW < nunits) id_next = __ldg(idrow + (u + NW) * UNIT + lane);
+        process_unit(a, id, qsrc, st, sl2, bad);
+    }
     if (__any_sync(0xffffffffu, bad) && lane == 0 && a.err) atomicOr(a.err, QSA_DEVERR_BAD_ID);
     quad_sum_l(st);
 
@@ -318,6 +384,268 @@ __global__ void __launch_bounds__(NW * 32) attn_fused_kernel(AttnLaunch a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Staged variant: each warp streams its 32-cell units through a private ring
+// of NS shared-memory stages filled by cp.async, NS-1 units ahead of the one
+// it computes, so the gathers' latency overlaps the tensor-core work without
+// holding the rows in registers.  Stage layout per unit: K codes [32][128]
+// with 16-byte chunk q of cell c at q ^ (c & 1); V codes [32][128] with chunk
+// q at q ^ (2 * ((c >> 1) & 3)) (both keep the fragment reads on distinct
+// banks); then ksc [32][4] and vsc [32][4] fp16.
+// ---------------------------------------------------------------------------
+constexpr int STAGE_BYTES = 2 * UNIT * D + 2 * UNIT * 8;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool pred) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(pred ? 16 : 0));
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src, bool pred) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src), "r"(pred ? 8 : 0));
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+// Issue the copies of one unit into stage `st` (shared address).  `id` is the
+// lane's id slot (already mapped to -1 when invalid).
+__device__ __forceinline__ void issue_unit(const AttnLaunch &a, int id, uint32_t st) {
+    const int lane = threadIdx.x & 31, q = lane & 7;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int cell = (lane >> 3) + 4 * i;
+        const int c = __shfl_sync(0xffffffffu, id, cell);
+        const bool ok = c >= 0;
+        const size_t off = (size_t)(ok ? c : 0) * D + 16 * q;
+        cp_async16(st + cell * D + ((q ^ (cell & 1)) << 4), a.kq + off, ok);
+        cp_async16(st + UNIT * D + cell * D + ((q ^ (2 * ((cell >> 1) & 3))) << 4), a.vq + off, ok);
+    }
+    const bool ok = id >= 0;
+    const size_t so = (size_t)(ok ? id : 0) * (D / G);
+    cp_async8(st + 2 * UNIT * D + lane * 8, a.ksc + so, ok);
+    cp_async8(st + 2 * UNIT * D + UNIT * 8 + lane * 8, a.vsc + so, ok);
+}
+
+// Compute one staged unit.  vmask: valid cells of the unit.
+template <class Q>
+__device__ __forceinline__ void compute_staged(const uint8_t *stp, unsigned vmask, const Q &qsrc, State &st,
+                                               float sl2) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
+    const uint8_t *K = stp, *V = stp + UNIT * D;
+    const __half *KS = reinterpret_cast<const __half *>(stp + 2 * UNIT * D);
+    const __half *VS = KS + UNIT * 4;
+
+    float s[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.0f;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        uint4 kd[4];
+        __half2 sc[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int cell = 8 * j + g;
+            kd[j] = *reinterpret_cast<const uint4 *>(K + cell * D + (((2 * r + half) ^ (cell & 1)) << 4));
+            sc[j] = __half2half2(KS[cell * 4 + r]);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            uint32_t qf[4];
+            qsrc.get(4 * half + kk, qf);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                __half2 lo, hi;
+                codes_to_h2(word_of(kd[j], kk) ^ 0x80808080u, lo, hi);
+                mma16816(s[j], qf, h2u(__hmul2(lo, sc[j])), h2u(__hmul2(hi, sc[j])));
+            }
+        }
+    }
+
+    float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const bool v = (vmask >> (8 * j + 2 * r + e)) & 1u;
+            s[j][e] = v ? s[j][e] * sl2 : -CUDART_INF_F;
+            s[j][e + 2] = v ? s[j][e + 2] * sl2 : -CUDART_INF_F;
+            mx0 = fmaxf(mx0, s[j][e]);
+            mx1 = fmaxf(mx1, s[j][e + 2]);
+        }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+    const float al0 = exp2f(st.m[0] - mn0), al1 = exp2f(st.m[1] - mn1);
+    st.m[0] = mn0;
+    st.m[1] = mn1;
+    float ps0 = 0.0f, ps1 = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            s[j][e] = exp2f(s[j][e] - mn0);
+            s[j][e + 2] = exp2f(s[j][e + 2] - mn1);
+            ps0 += s[j][e];
+            ps1 += s[j][e + 2];
+        }
+    st.l[0] = st.l[0] * al0 + ps0;
+    st.l[1] = st.l[1] * al1 + ps1;
+    if (__any_sync(0xffffffffu, al0 != 1.0f || al1 != 1.0f)) {
+#pragma unroll
+        for (int jd = 0; jd < 16; ++jd) {
+            st.o[jd][0] *= al0;
+            st.o[jd][1] *= al0;
+            st.o[jd][2] *= al1;
+            st.o[jd][3] *= al1;
+        }
+    }
+
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+        uint32_t pa[4];
+        pa[0] = h2u(__floats2half2_rn(s[2 * kk][0], s[2 * kk][1]));
+        pa[1] = h2u(__floats2half2_rn(s[2 * kk][2], s[2 * kk][3]));
+        pa[2] = h2u(__floats2half2_rn(s[2 * kk + 1][0], s[2 * kk + 1][1]));
+        pa[3] = h2u(__floats2half2_rn(s[2 * kk + 1][2], s[2 * kk + 1][3]));
+        uint4 vd[4];
+        __half vs[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int cell = 16 * kk + 2 * r + (e & 1) + 8 * (e >> 1);
+            vd[e] = *reinterpret_cast<const uint4 *>(V + cell * D + ((g ^ (2 * ((cell >> 1) & 3))) << 4));
+            vs[e] = VS[cell * 4 + (g >> 1)];
+        }
+        const __half2 v01 = __halves2half2(vs[0], vs[1]);
+        const __half2 v89 = __halves2half2(vs[2], vs[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t w0 = word_of(vd[0], i) ^ 0x80808080u, w1 = word_of(vd[1], i) ^ 0x80808080u;
+            const uint32_t w8 = word_of(vd[2], i) ^ 0x80808080u, w9 = word_of(vd[3], i) ^ 0x80808080u;
+            __half2 a0, a1, a2, a3, c0, c1, c2, c3;
+            codes_to_h2(prmt(w0, w1, 0x5140), a0, a1);
+            codes_to_h2(prmt(w0, w1, 0x7362), a2, a3);
+            codes_to_h2(prmt(w8, w9, 0x5140), c0, c1);
+            codes_to_h2(prmt(w8, w9, 0x7362), c2, c3);
+            mma16816(st.o[4 * i + 0], pa, h2u(__hmul2(a0, v01)), h2u(__hmul2(c0, v89)));
+            mma16816(st.o[4 * i + 1], pa, h2u(__hmul2(a1, v01)), h2u(__hmul2(c1, v89)));
+            mma16816(st.o[4 * i + 2], pa, h2u(__hmul2(a2, v01)), h2u(__hmul2(c2, v89)));
+            mma16816(st.o[4 * i + 3], pa, h2u(__hmul2(a3, v01)), h2u(__hmul2(c3, v89)));
+        }
+    }
+}
+
+#ifndef QSA_ATTN_NS
+#define QSA_ATTN_NS 2
+#endif
+
+template <int NW, int NS>
+__global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(AttnLaunch a) {
+    extern __shared__ __align__(16) uint8_t smem8[];
+    const int t = a.ntok - 1 - (int)blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
+    const float sl2 = a.softmax_scale * LOG2E;
+    const int32_t *idrow = a.ids + (size_t)t * a.width;
+    const int nunits = a.width / UNIT;
+    uint8_t *ring = smem8 + warp * NS * STAGE_BYTES;
+    const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+    uint8_t *sq = smem8 + NW * NS * STAGE_BYTES;  // Q rows in fragment order
+#if QSA_ATTN_QSMEM
+    stage_q(a, t, sq, NW * 32);
+    __syncthreads();
+    const QSmem qsrc{sq + g * QROW};
+#else
+    QRegs qsrc;
+    load_q(a, t, qsrc.qa);
+#endif
+    State st;
+    state_init(st);
+    bool bad = false;
+
+    // My units are u_i = warp + i*NW, i = 0 .. n-1.
+    const int n = warp < nunits ? (nunits - warp + NW - 1) / NW : 0;
+    auto unit_id = [&](int i) -> int {
+        if (i >= n) return -1;
+        int id = __ldg(idrow + (warp + i * NW) * UNIT + lane);
+        bad |= (id < -1) || (id >= a.cache_cells);
+        return (id >= 0 && id < a.cache_cells) ? id : -1;
+    };
+    int idq[NS];  // ids of units i .. i+NS-1 (ring of registers)
+#pragma unroll
+    for (int k = 0; k < NS; ++k) idq[k] = unit_id(k);
+#pragma unroll
+    for (int k = 0; k < NS - 1; ++k) {
+        if (__any_sync(0xffffffffu, idq[k] >= 0)) issue_unit(a, idq[k], ring_s + k * STAGE_BYTES);
+        cp_commit();
+    }
+    for (int i = 0; i < n; ++i) {
+        const int sI = i % NS;
+        const int sN = (i + NS - 1) % NS;
+        // ids of unit i are idq[i % NS] ... rotate: after use, refill with unit i+NS
+        int id_i = 0, id_n = 0;
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            if (k == sI) id_i = idq[k];
+            if (k == sN) id_n = idq[k];
+        }
+        if (__any_sync(0xffffffffu, id_n >= 0) && i + NS - 1 < n) issue_unit(a, id_n, ring_s + sN * STAGE_BYTES);
+        cp_commit();
+        cp_wait<NS - 1>();
+        __syncwarp();
+        const unsigned vmask = __ballot_sync(0xffffffffu, id_i >= 0);
+        if (vmask) compute_staged(ring + sI * STAGE_BYTES, vmask, qsrc, st, sl2);
+        __syncwarp();
+        const int nid = unit_id(i + NS);
+#pragma unroll
+        for (int k = 0; k < NS; ++k)
+            if (k == sI) idq[k] = nid;
+    }
+    cp_wait<0>();
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && a.err) atomicOr(a.err, QSA_DEVERR_BAD_ID);
+    quad_sum_l(st);
+    __syncthreads();
+
+    // Merge: reuse the rings (all copies have landed) for the per-warp states.
+    float *so = reinterpret_cast<float *>(smem8);
+    float *sm = so + NW * 16 * D;
+    float *sl = sm + NW * 16;
+    float *ow = so + warp * 16 * D;
+#pragma unroll
+    for (int jd = 0; jd < 16; ++jd) {
+        ow[g * D + 32 * r + jd] = st.o[jd][0];
+        ow[g * D + 32 * r + 16 + jd] = st.o[jd][1];
+        ow[(g + 8) * D + 32 * r + jd] = st.o[jd][2];
+        ow[(g + 8) * D + 32 * r + 16 + jd] = st.o[jd][3];
+    }
+    if (r == 0) {
+        sm[warp * 16 + g] = st.m[0];
+        sm[warp * 16 + g + 8] = st.m[1];
+        sl[warp * 16 + g] = st.l[0];
+        sl[warp * 16 + g + 8] = st.l[1];
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < a.n_q_heads * D; idx += NW * 32) {
+        const int h = idx / D, d = idx % D;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm[w * 16 + h]);
+        float res = 0.0f;
+        if (M != -CUDART_INF_F) {
+            float L = 0.0f, O = 0.0f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float mw = sm[w * 16 + h];
+                if (mw == -CUDART_INF_F) continue;
+                const float sc = exp2f(mw - M);
+                L += sc * sl[w * 16 + h];
+                O += sc * so[(w * 16 + h) * D + d];
+            }
+            res = O / L;
+        }
+        a.out[((size_t)t * a.n_q_heads + h) * D + d] = __half_as_ushort(__float2half_rn(res));
+    }
+}
+
 // Split path, part 1: one warp per (token, 64-cell chunk) writes the chunk's
 // unnormalised values, maximum (natural-log units) and denominator.
 template <int NW>
@@ -329,13 +657,14 @@ __global__ void __launch_bounds__(NW * 32) attn_chunk_kernel(AttnLaunch a) {
     if (c >= nch) return;
     const float sl2 = a.softmax_scale * LOG2E;
     const int32_t *idrow = a.ids + (size_t)t * a.width;
-    uint32_t qa[8][4];
-    load_q(a, t, qa);
+    QRegs qsrc;
+    load_q(a, t, qsrc.qa);
     State st;
     state_init(st);
     bool bad = false;
-    process_unit(a, idrow, c * CHUNK, qa, st, sl2, bad);
-    process_unit(a, idrow, c * CHUNK + UNIT, qa, st, sl2, bad);
+    const int id0 = __ldg(idrow + c * CHUNK + lane), id1 = __ldg(idrow + c * CHUNK + UNIT + lane);
+    process_unit(a, id0, qsrc, st, sl2, bad);
+    process_unit(a, id1, qsrc, st, sl2, bad);
     if (__any_sync(0xffffffffu, bad) && lane == 0 && a.err) atomicOr(a.err, QSA_DEVERR_BAD_ID);
     quad_sum_l(st);
 #pragma unroll
@@ -381,9 +710,21 @@ __global__ void __launch_bounds__(D) attn_merge_kernel(AttnLaunch a) {
     }
 }
 
+template <int NW, int NS>
+cudaError_t launch_staged(const AttnLaunch &a, cudaStream_t s) {
+    size_t smem = (size_t)NW * NS * STAGE_BYTES + 16 * QROW;
+    const size_t merge = (size_t)NW * (16 * D + 32) * sizeof(float);
+    if (smem < merge) smem = merge;
+    cudaError_t e = cudaFuncSetAttribute(attn_staged_kernel<NW, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    attn_staged_kernel<NW, NS><<<a.ntok, NW * 32, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <int NW>
 cudaError_t launch_fused(const AttnLaunch &a, cudaStream_t s) {
-    const size_t smem = (size_t)NW * (16 * D + 32) * sizeof(float);
+    const size_t smem = (size_t)NW * (16 * D + 32) * sizeof(float) + (QSA_ATTN_QSMEM ? 16 * QROW : 0);
     cudaError_t e = cudaFuncSetAttribute(attn_fused_kernel<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attn_fused_kernel<NW><<<a.ntok, NW * 32, smem, s>>>(a);
@@ -404,8 +745,18 @@ cudaError_t launch_attn(const AttnLaunch &a, cudaStream_t s) {
         attn_merge_kernel<<<a.ntok, D, 0, s>>>(a);
         return cudaGetLastError();
     }
+#ifndef QSA_ATTN_NW
+#define QSA_ATTN_NW 4
+#endif
+#ifndef QSA_ATTN_STAGED
+#define QSA_ATTN_STAGED 1
+#endif
+#if QSA_ATTN_STAGED
+    return launch_staged<QSA_ATTN_NW, QSA_ATTN_NS>(a, s);
+#else
     if (a.ntok < 64) return launch_fused<8>(a, s);
-    return launch_fused<4>(a, s);
+    return launch_fused<QSA_ATTN_NW>(a, s);
+#endif
 }
 
 }  // namespace qsa

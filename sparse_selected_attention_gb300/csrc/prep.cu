@@ -10,9 +10,13 @@
 // the K row and warp Hq+1 the V row.  With head_dim 128 every lane holds four
 // consecutive elements, so a row is one coalesced 512-byte load and a sum of
 // squares is five xor-shuffles.  The token's rotation angles are computed once
-// per CTA (in double, then reduced modulo 2*pi before the fp32 sincos) because
-// a single fp32 product p * inv_freq is off by up to 2e-3 rad at p ~ 32k.
+// per CTA (the product p * inv_freq exactly in double, reduced modulo 2*pi,
+// then an fp32 sincos) because a single fp32 product p * inv_freq is off by up
+// to 2e-3 rad at p ~ 32k.  The frequency table itself is computed once per
+// call on the host (GB300's fp64 rate makes a per-CTA pow expensive).
 #include <cuda_fp16.h>
+
+#include <cmath>
 
 #include "qsa_internal.h"
 
@@ -39,10 +43,21 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepParams P) {
     __shared__ float2 cs[D / 2];
     const int half = a.rope_dims >> 1;
 
+    // Issue this warp's row loads before the angle table is built.
+    const bool is_q = warp < a.n_q_heads, is_kv = !is_q && warp < a.n_q_heads + 2;
+    const bool is_v = warp == a.n_q_heads + 1;
+    const size_t row = ((size_t)t * a.n_q_heads + warp) * D;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), g = x;
+    if (is_q) {
+        x = __ldg(reinterpret_cast<const float4 *>(a.q_in + row) + lane);
+        g = __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane);
+    } else if (is_kv) {
+        x = __ldg(reinterpret_cast<const float4 *>((is_v ? a.v_in : a.k_in) + (size_t)t * D) + lane);
+    }
+
     if ((int)threadIdx.x < half) {
         const int i = threadIdx.x;
-        const float f = (float)pow((double)a.rope_theta, -2.0 * (double)i / (double)a.rope_dims);
-        const double ang = (double)(a.pos0 + t) * (double)f;  // exact: 24-bit x < 2^29
+        const double ang = (double)(a.pos0 + t) * (double)a.inv_freq[i];  // exact: 24-bit x < 2^29
         const double two_pi = 6.283185307179586;
         const double k = rint(ang * (1.0 / two_pi));
         const float r = (float)fma(-k, two_pi, ang);
@@ -52,10 +67,7 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepParams P) {
     }
     __syncthreads();
 
-    if (warp < a.n_q_heads) {
-        const size_t row = ((size_t)t * a.n_q_heads + warp) * D;
-        const float4 x = __ldg(reinterpret_cast<const float4 *>(a.q_in + row) + lane);
-        const float4 g = __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane);
+    if (is_q) {
         float ss = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
         ss = warp_sum(ss);
         const float rs = __frsqrt_rn(ss / (float)D + a.eps);
@@ -90,12 +102,9 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepParams P) {
         hv.y = *reinterpret_cast<const uint32_t *>(&h23);
         reinterpret_cast<uint2 *>(a.q_out + row)[lane] = hv;
         if (a.q_out_f32) reinterpret_cast<float4 *>(a.q_out_f32 + row)[lane] = make_float4(y[0], y[1], y[2], y[3]);
-    } else if (warp < a.n_q_heads + 2) {
-        const bool is_v = warp == a.n_q_heads + 1;
-        const float *src = (is_v ? a.v_in : a.k_in) + (size_t)t * D;
+    } else if (is_kv) {
         int8_t *dst = (is_v ? a.vq : a.kq) + (size_t)(a.pos0 + t) * D;
         uint16_t *sdst = (is_v ? a.vsc : a.ksc) + (size_t)(a.pos0 + t) * (D / G);
-        const float4 x = __ldg(reinterpret_cast<const float4 *>(src) + lane);
         float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -119,6 +128,8 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepParams P) {
 cudaError_t launch_prep(const PrepLaunch &a, cudaStream_t s) {
     if (a.ntok == 0) return cudaSuccess;
     PrepParams P{a};
+    for (int i = 0; i < a.rope_dims / 2; ++i)
+        P.a.inv_freq[i] = (float)std::pow((double)a.rope_theta, -2.0 * (double)i / (double)a.rope_dims);
     const int threads = 32 * (a.n_q_heads + 2);
     prep_kernel<<<a.ntok, threads, 0, s>>>(P);
     return cudaGetLastError();

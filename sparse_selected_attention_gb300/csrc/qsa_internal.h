@@ -11,6 +11,7 @@ namespace qsa {
 struct PrepLaunch {
     int ntok, pos0, n_q_heads, rope_dims;
     float eps, rope_theta;
+    float inv_freq[64];  // fp32(rope_theta^(-2i/rope_dims)), i < rope_dims/2, filled by the launcher
     const float *q_in, *k_in, *v_in, *norm_w;
     uint16_t *q_out;
     float *q_out_f32;

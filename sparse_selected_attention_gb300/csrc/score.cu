@@ -21,16 +21,22 @@
 // the causal cells; the others are never written.  Summing heads first cuts
 // the contraction twelvefold, so the pass is bound by its fp32 output writes.
 //
-// Kernel layout: one persistent 128-thread CTA per SM owns a contiguous range
-// of (token tile, cell tile) pairs.  Operands are written to shared memory by
-// the CTA's threads in the 128-byte-swizzled K-major layout and read by the
-// tensor core through shared-memory descriptors; accumulators are double
-// buffered in tensor memory (2 x 4 groups x 64 columns = 512 columns) so the
-// epilogue of tile i overlaps the MMAs of tile i+1.  Every mbarrier wait is
-// bounded; on expiry the kernel records QSA_DEVERR_TIMEOUT, stops, frees its
-// tensor memory and returns.
+// Kernel layout: one persistent CTA per SM owns a contiguous range of
+// (token tile, cell tile) pairs and runs it as a warp-specialised pipeline:
+// two producer warps convert int8 codes to fp16 into a ring of four A stages
+// (and copy qbar hi/lo into one of two B buffers when the token tile
+// changes), one thread issues the tcgen05 MMAs into one of two accumulator
+// sets in tensor memory (2 x 4 groups x 64 columns = 512 columns), and four
+// epilogue warps drain the other set to global memory.  Operands use the
+// 128-byte-swizzled K-major layout read through shared-memory descriptors.
+// Every mbarrier wait is bounded; on expiry the kernel records
+// QSA_DEVERR_TIMEOUT, all roles stop, tensor memory is freed and the kernel
+// returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "qsa.h"
@@ -43,19 +49,30 @@ constexpr int D = 128;
 constexpr int NG = 4;        // 32-dim scale groups
 constexpr int TM = 128;      // cells per tile (MMA M)
 constexpr int TN = 64;       // tokens per tile (MMA N)
-constexpr int THREADS = 128;
+constexpr int NEPI = 4;      // epilogue warps 0..3
+constexpr int NPROD = 2;     // producer warps 4..5
+constexpr int MMA_WARP = 6;  // TMEM owner / MMA issuer
+constexpr int THREADS = 32 * 7;
+constexpr int NA = 3;        // A stages
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_BYTES = TM * D * 2;        // fp16, two 64-wide K blocks
 constexpr uint32_t A_KBLOCK = TM * 128;         // bytes of one 64-wide K block
-constexpr uint32_t B_BYTES = TN * D * 2;
+constexpr uint32_t B_BYTES = TN * D * 2;        // one of qbar hi / lo
 constexpr uint32_t B_KBLOCK = TN * 128;
-constexpr uint32_t SMEM_USED = 2 * A_BYTES + 2 * B_BYTES + 64;
-// Ask for more than half of an SM's shared memory so exactly one CTA (and one
-// 512-column tensor-memory allocation) lives on each SM.
-constexpr uint32_t SMEM_ALLOC = 120 * 1024;
+constexpr uint32_t B_PAIR = 2 * B_BYTES;        // hi + lo of one token tile
+constexpr uint32_t C_BYTES = TN * TM * 4;       // fp32 output tile, token-major
+constexpr uint32_t OFF_B = NA * A_BYTES;
+constexpr uint32_t OFF_C = OFF_B + 2 * B_PAIR;
+constexpr uint32_t OFF_BAR = OFF_C + 2 * C_BYTES;
+constexpr uint32_t OFF_FLAG = OFF_BAR + (2 * NA + 8) * 8;
+constexpr uint32_t SMEM_USED = OFF_FLAG + 16;
+// The layout needs more than half of an SM's shared memory, so exactly one
+// CTA (and one 512-column tensor-memory allocation) lives on each SM.
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 constexpr long long WAIT_LIMIT = 1ll << 24;     // mbarrier polls before giving up
 
-static_assert(SMEM_USED + 1024 <= SMEM_ALLOC, "shared memory layout");
+static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory layout");
+
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -176,24 +193,89 @@ __device__ __forceinline__ int cell_tiles(const ScoreLaunch &a, int tt) {
     return (a.pos0 + tl) / TM + 1;
 }
 
-__global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a) {
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+// Two fp32 fused multiply-adds in one instruction: (a.lo*b.lo + c.lo, a.hi*b.hi + c.hi).
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ void named_sync_epilogue() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+struct Walker {
+    int tt, ct, ncur;
+};
+
+__device__ __forceinline__ void walk_next(const ScoreLaunch &a, Walker &w) {
+    if (++w.ct >= w.ncur) {
+        w.ct = 0;
+        ++w.tt;
+        w.ncur = cell_tiles(a, w.tt);
+    }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait that also gives up as soon as another role has given up.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort) {
+    for (long long i = 0; i < WAIT_LIMIT; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255) == 255 && *abort) return false;
+    }
+    *abort = 1;
+    return false;
+}
+
+// Warp roles: warps 0-3 drain the accumulators (epilogue; warp w owns TMEM
+// lanes 32w..32w+31, i.e. cells 32w.. of the tile), warps 4-5 produce the
+// operands (int8 codes -> fp16 A stages, qbar hi/lo -> B buffers), warp 6
+// allocates tensor memory and one of its threads issues the MMAs.  Stages
+// are handed over with mbarriers: a_full / a_empty (NA A stages), b_full /
+// b_empty (2 B buffers, one per token tile in flight), acc_full / acc_empty
+// (2 TMEM accumulator sets).
+__global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const __grid_constant__ CUtensorMap tmap,
+                                                            int use_tma) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t sA0 = base, sB0 = base + 2 * A_BYTES;
-    const uint32_t bar0 = sB0 + 2 * B_BYTES;  // two 8-byte mbarriers
-    uint8_t *gen = smem_raw + (base - raw);   // generic pointer to `base`
-    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gen + 2 * A_BYTES + 2 * B_BYTES + 16);
-
+    uint8_t *gen = smem_raw + (base - raw);
+    const uint32_t sA = base, sB = base + OFF_B, sC = base + OFF_C, bar = base + OFF_BAR;
+    const uint32_t a_full = bar, a_empty = bar + 8 * NA, b_full = bar + 16 * NA, b_empty = b_full + 16,
+                   acc_full = b_empty + 16, acc_empty = acc_full + 16;
+    volatile int *abort = reinterpret_cast<volatile int *>(gen + OFF_FLAG);
+    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gen + OFF_FLAG + 8);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        mbar_init(bar0, 1);
-        mbar_init(bar0 + 8, 1);
+        for (int i = 0; i < NA; ++i) {
+            mbar_init(a_full + 8 * i, NPROD * 32);
+            mbar_init(a_empty + 8 * i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(b_full + 8 * i, NPROD * 32);
+            mbar_init(b_empty + 8 * i, 1);
+            mbar_init(acc_full + 8 * i, 1);
+            mbar_init(acc_empty + 8 * i, NEPI * 32);
+        }
+        *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((const void *)tslot)),
+    if (warp == MMA_WARP) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32((const void *)tslot)),
                      "r"(TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
@@ -202,168 +284,231 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a) {
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    // Contiguous share of the linear (token tile, cell tile) sequence.
+    // This CTA's contiguous share of the (token tile, cell tile) sequence.
     const int ntt = (a.ntok + TN - 1) / TN;
     long long total = 0;
     for (int tt = 0; tt < ntt; ++tt) total += cell_tiles(a, tt);
     const long long begin = total * blockIdx.x / gridDim.x;
     const long long end = total * (blockIdx.x + 1) / gridDim.x;
-    TileWalk cur{0, 0};
+    const int n = (int)(end - begin);
+    Walker w0{0, 0, 0};
     {
         long long k = begin;
-        while (cur.tt < ntt && k >= cell_tiles(a, cur.tt)) {
-            k -= cell_tiles(a, cur.tt);
-            ++cur.tt;
+        while (w0.tt < ntt && k >= cell_tiles(a, w0.tt)) {
+            k -= cell_tiles(a, w0.tt);
+            ++w0.tt;
         }
-        cur.ct = (int)k;
+        w0.ct = (int)k;
+        w0.ncur = cell_tiles(a, w0.tt);
     }
 
-    // Prefetch registers for the next A tile: 8 x 16 bytes of int8 codes.
-    uint4 pre[8];
-    auto load_a = [&](const TileWalk &w) {
+    if (warp >= NEPI && warp < NEPI + NPROD) {
+        // ---- producers ----
+        const int pt = tid - NEPI * 32;
+        Walker w = w0;
+        int nb = 0, cur_tt = -1;
+        uint4 pre[16];
+        auto load_a = [&](int ct) {
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-            const int q = it * THREADS + tid, m = q >> 3, dc = q & 7;
-            const int c = w.ct * TM + m;
-            pre[it] = c < a.cache_cells ? __ldg(reinterpret_cast<const uint4 *>(a.kq + (size_t)c * D) + dc)
-                                        : make_uint4(0x0u, 0x0u, 0x0u, 0x0u);
-        }
-    };
-    auto store_a = [&](uint32_t sA) {
+            for (int it = 0; it < 16; ++it) {
+                const int q = it * (NPROD * 32) + pt, m = q >> 3, dc = q & 7;
+                const int c = ct * TM + m;
+                pre[it] = c < a.cache_cells ? __ldg(reinterpret_cast<const uint4 *>(a.kq + (size_t)c * D) + dc)
+                                            : make_uint4(0u, 0u, 0u, 0u);
+            }
+        };
+        if (n > 0) load_a(w.ct);
+        for (int k = 0; k < n; ++k) {
+            if (w.tt != cur_tt) {
+                const int bs = nb & 1;
+                if (nb >= 2 && !mbar_wait_or_abort(b_empty + 8 * bs, ((nb >> 1) - 1) & 1, abort)) break;
+                const uint32_t dstB = sB + bs * B_PAIR;
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-            const int q = it * THREADS + tid, m = q >> 3, dc = q & 7;
-            uint32_t h[8];
-            codes_to_h2(pre[it].x ^ 0x80808080u, h[0], h[1]);
-            codes_to_h2(pre[it].y ^ 0x80808080u, h[2], h[3]);
-            codes_to_h2(pre[it].z ^ 0x80808080u, h[4], h[5]);
-            codes_to_h2(pre[it].w ^ 0x80808080u, h[6], h[7]);
-            const int kb = dc >> 2, cc = 2 * (dc & 3);
-            const uint32_t row = sA + kb * A_KBLOCK + (m >> 3) * 1024 + (m & 7) * 128;
-            const uint32_t p0 = row + (((cc) ^ (m & 7)) << 4), p1 = row + (((cc + 1) ^ (m & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(p0), "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]));
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(p1), "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]));
-        }
-    };
-    auto load_b = [&](int tt) {
-        // qbar hi (part 0) and lo (part 1) rows of this token tile.
-#pragma unroll 4
-        for (int it = 0; it < 16; ++it) {
-            const int q = it * THREADS + tid, part = q >> 10, n = (q & 1023) >> 4, ci = q & 15;
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.qsum + ((size_t)(tt * TN + n) * 2 + part) * D) + ci);
-            const int kb = ci >> 3, cc = ci & 7;
-            const uint32_t p = sB0 + part * B_BYTES + kb * B_KBLOCK + (n >> 3) * 1024 + (n & 7) * 128 + ((cc ^ (n & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
-        }
-    };
-
-    bool timeout = false;
-    auto epilogue = [&](const TileWalk &w, int k) {
-        const int b = k & 1;
-        if (!mbar_wait(bar0 + 8 * b, (uint32_t)((k >> 1) & 1))) {
-            timeout = true;
-            return;
-        }
-        tc_fence_after();
-        const int cell = w.ct * TM + warp * 32 + lane;
-        float ks[NG] = {0.f, 0.f, 0.f, 0.f};
-        if (cell < a.cache_cells) {
-            const uint2 kv = __ldg(reinterpret_cast<const uint2 *>(a.ksc + (size_t)cell * NG));
-            ks[0] = __half2float(__ushort_as_half((unsigned short)(kv.x & 0xFFFF)));
-            ks[1] = __half2float(__ushort_as_half((unsigned short)(kv.x >> 16)));
-            ks[2] = __half2float(__ushort_as_half((unsigned short)(kv.y & 0xFFFF)));
-            ks[3] = __half2float(__ushort_as_half((unsigned short)(kv.y >> 16)));
-        }
-        const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * NG * TN);
-#pragma unroll 1
-        for (int j0 = 0; j0 < TN; j0 += 16) {
-            const int t0 = w.tt * TN + j0;
-            if (t0 >= a.ntok) break;  // warp-uniform
-            uint32_t v[NG][16];
+                for (int half = 0; half < 2; ++half) {
+                    uint4 v[16];
 #pragma unroll
-            for (int g = 0; g < NG; ++g) tmem_ld16(tbase + g * TN + j0, v[g]);
-            tmem_wait_ld();
+                    for (int it = 0; it < 16; ++it) {
+                        const int q = (half * 16 + it) * (NPROD * 32) + pt, part = q >> 10, row = (q & 1023) >> 4,
+                                  ci = q & 15;
+                        v[it] = __ldg(reinterpret_cast<const uint4 *>(
+                                          a.qsum + ((size_t)(w.tt * TN + row) * 2 + part) * D) + ci);
+                    }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int t = t0 + j;
-                if (t < a.ntok && cell <= a.pos0 + t) {
-                    float s = ks[0] * __uint_as_float(v[0][j]);
-                    s = fmaf(ks[1], __uint_as_float(v[1][j]), s);
-                    s = fmaf(ks[2], __uint_as_float(v[2][j]), s);
-                    s = fmaf(ks[3], __uint_as_float(v[3][j]), s);
-                    a.scores[(size_t)t * a.ld + cell] = s;
+                    for (int it = 0; it < 16; ++it) {
+                        const int q = (half * 16 + it) * (NPROD * 32) + pt, part = q >> 10, row = (q & 1023) >> 4,
+                                  ci = q & 15;
+                        const int kb = ci >> 3, cc = ci & 7;
+                        const uint32_t p = dstB + part * B_BYTES + kb * B_KBLOCK + (row >> 3) * 1024 +
+                                           (row & 7) * 128 + ((cc ^ (row & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(p), "r"(v[it].x), "r"(v[it].y),
+                                     "r"(v[it].z), "r"(v[it].w));
+                    }
                 }
+                fence_async_smem();
+                mbar_arrive(b_full + 8 * bs);
+                ++nb;
+                cur_tt = w.tt;
+            }
+            const int st = k % NA;
+            if (k >= NA && !mbar_wait_or_abort(a_empty + 8 * st, ((k / NA) - 1) & 1, abort)) break;
+            const uint32_t dstA = sA + st * A_BYTES;
+#pragma unroll
+            for (int it = 0; it < 16; ++it) {
+                const int q = it * (NPROD * 32) + pt, m = q >> 3, dc = q & 7;
+                uint32_t h[8];
+                codes_to_h2(pre[it].x ^ 0x80808080u, h[0], h[1]);
+                codes_to_h2(pre[it].y ^ 0x80808080u, h[2], h[3]);
+                codes_to_h2(pre[it].z ^ 0x80808080u, h[4], h[5]);
+                codes_to_h2(pre[it].w ^ 0x80808080u, h[6], h[7]);
+                const int kb = dc >> 2, cc = 2 * (dc & 3);
+                const uint32_t row = dstA + kb * A_KBLOCK + (m >> 3) * 1024 + (m & 7) * 128;
+                const uint32_t p0 = row + ((cc ^ (m & 7)) << 4), p1 = row + (((cc + 1) ^ (m & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(p0), "r"(h[0]), "r"(h[1]), "r"(h[2]),
+                             "r"(h[3]));
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(p1), "r"(h[4]), "r"(h[5]), "r"(h[6]),
+                             "r"(h[7]));
+            }
+            fence_async_smem();
+            mbar_arrive(a_full + 8 * st);
+            walk_next(a, w);
+            if (k + 1 < n) load_a(w.ct);
+        }
+    } else if (warp == MMA_WARP) {
+        // ---- MMA issuer ----
+        if (lane == 0) {
+            Walker w = w0;
+            int nb = 0, cur_tt = -1, bs = 0;
+            for (int k = 0; k < n; ++k) {
+                if (w.tt != cur_tt) {
+                    bs = nb & 1;
+                    if (!mbar_wait_or_abort(b_full + 8 * bs, (nb >> 1) & 1, abort)) break;
+                    ++nb;
+                    cur_tt = w.tt;
+                }
+                const int st = k % NA, b = k & 1;
+                if (!mbar_wait_or_abort(a_full + 8 * st, (k / NA) & 1, abort)) break;
+                if (k >= 2 && !mbar_wait_or_abort(acc_empty + 8 * b, ((k >> 1) - 1) & 1, abort)) break;
+                tc_fence_after();
+                const uint32_t aS = sA + st * A_BYTES, bS = sB + bs * B_PAIR;
+#pragma unroll
+                for (int g = 0; g < NG; ++g) {
+                    const uint32_t dt = tmem + (uint32_t)(b * NG * TN + g * TN);
+#pragma unroll
+                    for (int s2 = 0; s2 < 2; ++s2) {
+                        const int ksx = 2 * g + s2, kb = ksx >> 2;
+                        const uint32_t koff = (ksx & 3) * 32;
+                        const uint64_t ad = sw128_desc(aS + kb * A_KBLOCK + koff);
+#pragma unroll
+                        for (int part = 0; part < 2; ++part) {
+                            const uint64_t bd = sw128_desc(bS + part * B_BYTES + kb * B_KBLOCK + koff);
+                            mma_f16(dt, ad, bd, (s2 | part) ? 1u : 0u);
+                        }
+                    }
+                }
+                mma_commit(a_empty + 8 * st);
+                mma_commit(acc_full + 8 * b);
+                Walker nx = w;
+                walk_next(a, nx);
+                if (k + 1 == n || nx.tt != w.tt) mma_commit(b_empty + 8 * bs);
+                w = nx;
             }
         }
-        tc_fence_before();
-    };
-
-    TileWalk prev{-1, -1};
-    int cur_tt = -1;
-    bool pending = false;
-    const long long n = end - begin;
-    if (n > 0) load_a(cur);
-    for (long long k = 0; k < n; ++k) {
-        if (__syncthreads_or(timeout ? 1 : 0)) {
-            timeout = true;
-            break;
-        }
-        const int b = (int)(k & 1);
-        if (cur.tt != cur_tt) {
-            if (pending) {  // the MMAs still reading the old B must finish first
-                epilogue(prev, (int)(k - 1));
-                pending = false;
-                if (__syncthreads_or(timeout ? 1 : 0)) {
-                    timeout = true;
-                    break;
-                }
-            }
-            load_b(cur.tt);
-            cur_tt = cur.tt;
-        }
-        store_a(sA0 + b * A_BYTES);
-        TileWalk next = cur;
-        if (++next.ct >= cell_tiles(a, next.tt)) {
-            next.ct = 0;
-            ++next.tt;
-        }
-        if (k + 1 < n) load_a(next);
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
+    } else if (warp < NEPI) {
+        // ---- epilogue ----
+        // Fully causal tiles are combined into a token-major fp32 tile in
+        // shared memory and written by one TMA bulk-tensor store; tiles that
+        // cross the causal boundary are stored element-wise under the mask.
+        Walker w = w0;
+        int nfull = 0;
+        for (int k = 0; k < n; ++k) {
+            const int b = k & 1;
+            const int c0 = w.ct * TM, t0 = w.tt * TN;
+            const bool full = use_tma && (c0 + TM - 1 <= a.pos0 + t0);
+            const int cell = c0 + warp * 32 + lane;
+            uint2 kv = make_uint2(0u, 0u);
+            if (cell < a.cache_cells) kv = __ldg(reinterpret_cast<const uint2 *>(a.ksc + (size_t)cell * NG));
+            if (!mbar_wait_or_abort(acc_full + 8 * b, (k >> 1) & 1, abort)) break;
             tc_fence_after();
-            const uint32_t sA = sA0 + b * A_BYTES;
+            const float ks0 = __half2float(__ushort_as_half((unsigned short)(kv.x & 0xFFFF)));
+            const float ks1 = __half2float(__ushort_as_half((unsigned short)(kv.x >> 16)));
+            const float ks2 = __half2float(__ushort_as_half((unsigned short)(kv.y & 0xFFFF)));
+            const float ks3 = __half2float(__ushort_as_half((unsigned short)(kv.y >> 16)));
+            const uint64_t k0 = pack2(ks0, ks0), k1 = pack2(ks1, ks1), k2 = pack2(ks2, ks2), k3 = pack2(ks3, ks3);
+            const uint32_t cbuf = sC + (nfull & 1) * C_BYTES;
+            if (full) {
+                // The store issued two full tiles ago read this buffer.
+                if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                named_sync_epilogue();
+            }
+            const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * NG * TN);
+            const int tmin = cell - a.pos0;  // first token whose causal range reaches `cell`
+#pragma unroll 1
+            for (int j0 = 0; j0 < TN; j0 += 16) {
+                if (!full && t0 + j0 >= a.ntok) break;  // warp-uniform
+                uint32_t v[NG][16];
 #pragma unroll
-            for (int g = 0; g < NG; ++g) {
-                const uint32_t dt = tmem + (uint32_t)(b * NG * TN + g * TN);
+                for (int g = 0; g < NG; ++g) tmem_ld16(tbase + g * TN + j0, v[g]);
+                tmem_wait_ld();
+                float o[16];
 #pragma unroll
-                for (int s = 0; s < 2; ++s) {
-                    const int ksx = 2 * g + s, kb = ksx >> 2;
-                    const uint32_t koff = (ksx & 3) * 32;
-                    const uint64_t ad = sw128_desc(sA + kb * A_KBLOCK + koff);
+                for (int j = 0; j < 16; j += 2) {
+                    uint64_t acc = fma2(k0, pack2(__uint_as_float(v[0][j]), __uint_as_float(v[0][j + 1])), 0ull);
+                    acc = fma2(k1, pack2(__uint_as_float(v[1][j]), __uint_as_float(v[1][j + 1])), acc);
+                    acc = fma2(k2, pack2(__uint_as_float(v[2][j]), __uint_as_float(v[2][j + 1])), acc);
+                    acc = fma2(k3, pack2(__uint_as_float(v[3][j]), __uint_as_float(v[3][j + 1])), acc);
+                    o[j] = __uint_as_float((uint32_t)acc);
+                    o[j + 1] = __uint_as_float((uint32_t)(acc >> 32));
+                }
+                if (full) {
+                    const uint32_t dst = cbuf + (uint32_t)(j0 * TM + warp * 32 + lane) * 4;
 #pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        const uint64_t bd = sw128_desc(sB0 + part * B_BYTES + kb * B_KBLOCK + koff);
-                        mma_f16(dt, ad, bd, (s | part) ? 1u : 0u);
+                    for (int j = 0; j < 16; ++j)
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + j * TM * 4), "f"(o[j]) : "memory");
+                } else {
+                    float *dst = a.scores + (size_t)(t0 + j0) * a.ld + cell;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int t = t0 + j0 + j;
+                        if (t < a.ntok && t >= tmin) dst[(size_t)j * a.ld] = o[j];
                     }
                 }
             }
-            mma_commit(bar0 + 8 * b);
+            tc_fence_before();
+            mbar_arrive(acc_empty + 8 * b);
+            if (full) {
+                fence_async_smem();
+                named_sync_epilogue();
+                if (tid == 0) tma_store_2d(&tmap, c0, t0, cbuf);
+                ++nfull;
+            }
+            walk_next(a, w);
         }
-        if (pending) epilogue(prev, (int)(k - 1));
-        prev = cur;
-        pending = true;
-        cur = next;
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
-    if (pending && !timeout) epilogue(prev, (int)(n - 1));
-    if (timeout && a.err && lane == 0) atomicOr(a.err, QSA_DEVERR_TIMEOUT);
+
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (tid == 0 && *abort && a.err) atomicOr(a.err, QSA_DEVERR_TIMEOUT);
+    if (warp == MMA_WARP) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
     }
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link-time dependency on libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
 }
 
 }  // namespace
@@ -388,7 +533,24 @@ cudaError_t launch_score(const ScoreLaunch &a, cudaStream_t s) {
     const int grid = (int)(total < sms ? total : sms);
     e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    score_kernel<<<grid, THREADS, SMEM_ALLOC, s>>>(a);
+    // Tensor map of the score rows for the TMA stores of fully causal tiles.
+    // It needs 16-byte aligned rows; otherwise every tile takes the masked
+    // element-wise path.
+    CUtensorMap map;
+    std::memset(&map, 0, sizeof map);
+    int use_tma = 0;
+    if (a.ld % 4 == 0 && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0) {
+        if (auto encode = tensor_map_encoder()) {
+            const cuuint64_t dims[2] = {(cuuint64_t)a.ld, (cuuint64_t)a.ntok};
+            const cuuint64_t strides[1] = {(cuuint64_t)a.ld * sizeof(float)};
+            const cuuint32_t box[2] = {(cuuint32_t)TM, (cuuint32_t)TN};
+            const cuuint32_t estr[2] = {1, 1};
+            use_tma = encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.scores, dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        }
+    }
+    score_kernel<<<grid, THREADS, SMEM_ALLOC, s>>>(a, map, use_tma);
     return cudaGetLastError();
 }
 
