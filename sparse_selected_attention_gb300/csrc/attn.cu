@@ -12,17 +12,18 @@
 // GB300 design.  The 12 query heads share one KV row, so a cell's K and V
 // codes are gathered once and used for every head: the head dimension is the
 // M side (padded 12 -> 16) of m16n8k16 tensor-core products, cells are N for
-// Q.K^T and the contraction for P.V.  Gathered int8 rows are loaded straight
-// from global memory into the registers that form the mma fragments (no shared
-// memory staging): a permutation of the contraction index d makes each
-// thread's part of a K row one contiguous 32-byte span and its part of a V row
-// one contiguous 16-byte span, so every gather is a coalesced 16-byte load.
-// Codes are turned into exact fp16 integers with a byte-permute bias trick and
+// Q.K^T and the contraction for P.V.  A permutation of the contraction index d
+// makes each thread's part of a K row one contiguous 32-byte span (group r of
+// the row for quad lane r) and its part of a V row one contiguous 16-byte span,
+// so fragments are read with 16-byte shared-memory loads.  Codes are turned
+// into exact fp16 integers with a byte-permute bias trick (0x64xx - 1152) and
 // scaled by their fp16 group scale in the same registers.  Padding slots are
-// never dereferenced: their scores are -inf and their values zero.
+// never dereferenced: cp.async zero-fills them, scores are -inf, values zero.
 //
-// Fused path (part == NULL): one CTA per token, NW warps; each warp walks its
-// share of 32-cell units with an online max / denominator, and the warps' states
+// Fused path (part == NULL): one CTA per token, four warps; each warp streams
+// its share of 32-cell units through a private two-stage shared-memory ring
+// filled by cp.async (rows swizzled by 16-byte chunk so fragment reads are
+// bank-conflict free), with an online max / denominator, and the warps' states
 // are merged max-first in shared memory.  Split path (part != NULL): one warp
 // per 64-cell chunk writes that chunk's (o_c, m_c, l_c); a second kernel merges
 // the chunks max-first exactly as the definition states.
@@ -129,35 +130,6 @@ struct QRegs {
         f[3] = qa[k][3];
     }
 };
-
-// Q fragments read from shared memory, stored in fragment order: row h,
-// k-step k, quad lane r -> 8 bytes at h * QROW + (4k + r) * 8.  The 288-byte
-// row pitch keeps a half-warp's 8-byte reads on distinct banks.
-constexpr int QROW = 288;
-struct QSmem {
-    const uint8_t *base;  // this thread's row g
-    __device__ __forceinline__ void get(int k, uint32_t (&f)[4]) const {
-        const int r = threadIdx.x & 3;
-        const uint2 lo = *reinterpret_cast<const uint2 *>(base + (4 * k + r) * 8);
-        const uint2 hi = *reinterpret_cast<const uint2 *>(base + 8 * QROW + (4 * k + r) * 8);
-        f[0] = lo.x;
-        f[1] = hi.x;
-        f[2] = lo.y;
-        f[3] = hi.y;
-    }
-};
-
-// Stage token t's Q rows (all 16 head rows, zeros past n_q_heads) in shared
-// memory in fragment order.  Called by every thread of the CTA.
-__device__ __forceinline__ void stage_q(const AttnLaunch &a, int t, uint8_t *sq, int nthreads) {
-    for (int i = threadIdx.x; i < 16 * 32; i += nthreads) {
-        const int h = i >> 5, k = (i >> 2) & 7, r = i & 3;
-        uint2 v = make_uint2(0u, 0u);
-        if (h < a.n_q_heads)
-            v = __ldg(reinterpret_cast<const uint2 *>(a.q + ((size_t)t * a.n_q_heads + h) * D + 32 * r + 4 * k));
-        *reinterpret_cast<uint2 *>(sq + h * QROW + (4 * k + r) * 8) = v;
-    }
-}
 
 // One 32-cell unit (id slots slot0 .. slot0+31, lane's id already loaded)
 // folded into the warp's state.  sl2 = softmax_scale * log2(e).  Sets `bad`
@@ -306,86 +278,9 @@ __device__ __forceinline__ void quad_sum_l(State &st) {
 #ifndef QSA_ATTN_MINB
 #define QSA_ATTN_MINB 3
 #endif
-#ifndef QSA_ATTN_QSMEM
-#define QSA_ATTN_QSMEM 0
-#endif
-
-template <int NW>
-__global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_fused_kernel(AttnLaunch a) {
-    extern __shared__ float smem[];
-    float *so = smem;                       // [NW][16][D]
-    float *sm = smem + NW * 16 * D;         // [NW][16]
-    float *sl = sm + NW * 16;               // [NW][16]
-    const int t = a.ntok - 1 - (int)blockIdx.x;  // longest lists first when lists grow with t
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
-    const float sl2 = a.softmax_scale * LOG2E;
-    const int32_t *idrow = a.ids + (size_t)t * a.width;
-    const int nunits = a.width / UNIT;
-
-#if QSA_ATTN_QSMEM
-    uint8_t *sq = reinterpret_cast<uint8_t *>(sl + NW * 16);
-    stage_q(a, t, sq, NW * 32);
-    __syncthreads();
-    const QSmem qsrc{sq + g * QROW};
-#else
-    QRegs qsrc;
-    load_q(a, t, qsrc.qa);
-#endif
-    State st;
-    state_init(st);
-    bool bad = false;
-    // The next unit's id is loaded one unit ahead, so each unit's critical
-    // path holds one dependent global load (the row gather), not two.
-    int id_next = warp < nunits ? __ldg(idrow + warp * UNIT + lane) : -1;
-    for (int u = warp; u < nunits; u += NW) {
-        const int id = id_next;
-        if (u + NW < nunits) id_next = __ldg(idrow + (u + NW) * UNIT + lane);
-        process_unit(a, id, qsrc, st, sl2, bad);
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0 && a.err) atomicOr(a.err, QSA_DEVERR_BAD_ID);
-    quad_sum_l(st);
-
-    float *ow = so + warp * 16 * D;
-#pragma unroll
-    for (int jd = 0; jd < 16; ++jd) {
-        ow[g * D + 32 * r + jd] = st.o[jd][0];
-        ow[g * D + 32 * r + 16 + jd] = st.o[jd][1];
-        ow[(g + 8) * D + 32 * r + jd] = st.o[jd][2];
-        ow[(g + 8) * D + 32 * r + 16 + jd] = st.o[jd][3];
-    }
-    if (r == 0) {
-        sm[warp * 16 + g] = st.m[0];
-        sm[warp * 16 + g + 8] = st.m[1];
-        sl[warp * 16 + g] = st.l[0];
-        sl[warp * 16 + g + 8] = st.l[1];
-    }
-    __syncthreads();
-
-    // Max-first merge of the warps' states.
-    for (int idx = threadIdx.x; idx < a.n_q_heads * D; idx += NW * 32) {
-        const int h = idx / D, d = idx % D;
-        float M = -CUDART_INF_F;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm[w * 16 + h]);
-        float res = 0.0f;
-        if (M != -CUDART_INF_F) {
-            float L = 0.0f, O = 0.0f;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float mw = sm[w * 16 + h];
-                if (mw == -CUDART_INF_F) continue;
-                const float sc = exp2f(mw - M);
-                L += sc * sl[w * 16 + h];
-                O += sc * so[(w * 16 + h) * D + d];
-            }
-            res = O / L;
-        }
-        a.out[((size_t)t * a.n_q_heads + h) * D + d] = __half_as_ushort(__float2half_rn(res));
-    }
-}
 
 // ---------------------------------------------------------------------------
-// Staged variant: each warp streams its 32-cell units through a private ring
+// Fused kernel: each warp streams its 32-cell units through a private ring
 // of NS shared-memory stages filled by cp.async, NS-1 units ahead of the one
 // it computes, so the gathers' latency overlaps the tensor-core work without
 // holding the rows in registers.  Stage layout per unit: K codes [32][128]
@@ -549,15 +444,8 @@ __global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(Att
     const int nunits = a.width / UNIT;
     uint8_t *ring = smem8 + warp * NS * STAGE_BYTES;
     const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
-    uint8_t *sq = smem8 + NW * NS * STAGE_BYTES;  // Q rows in fragment order
-#if QSA_ATTN_QSMEM
-    stage_q(a, t, sq, NW * 32);
-    __syncthreads();
-    const QSmem qsrc{sq + g * QROW};
-#else
     QRegs qsrc;
     load_q(a, t, qsrc.qa);
-#endif
     State st;
     state_init(st);
     bool bad = false;
@@ -712,22 +600,13 @@ __global__ void __launch_bounds__(D) attn_merge_kernel(AttnLaunch a) {
 
 template <int NW, int NS>
 cudaError_t launch_staged(const AttnLaunch &a, cudaStream_t s) {
-    size_t smem = (size_t)NW * NS * STAGE_BYTES + 16 * QROW;
+    size_t smem = (size_t)NW * NS * STAGE_BYTES;
     const size_t merge = (size_t)NW * (16 * D + 32) * sizeof(float);
     if (smem < merge) smem = merge;
     cudaError_t e = cudaFuncSetAttribute(attn_staged_kernel<NW, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     attn_staged_kernel<NW, NS><<<a.ntok, NW * 32, smem, s>>>(a);
-    return cudaGetLastError();
-}
-
-template <int NW>
-cudaError_t launch_fused(const AttnLaunch &a, cudaStream_t s) {
-    const size_t smem = (size_t)NW * (16 * D + 32) * sizeof(float) + (QSA_ATTN_QSMEM ? 16 * QROW : 0);
-    cudaError_t e = cudaFuncSetAttribute(attn_fused_kernel<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attn_fused_kernel<NW><<<a.ntok, NW * 32, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -748,15 +627,7 @@ cudaError_t launch_attn(const AttnLaunch &a, cudaStream_t s) {
 #ifndef QSA_ATTN_NW
 #define QSA_ATTN_NW 4
 #endif
-#ifndef QSA_ATTN_STAGED
-#define QSA_ATTN_STAGED 1
-#endif
-#if QSA_ATTN_STAGED
     return launch_staged<QSA_ATTN_NW, QSA_ATTN_NS>(a, s);
-#else
-    if (a.ntok < 64) return launch_fused<8>(a, s);
-    return launch_fused<QSA_ATTN_NW>(a, s);
-#endif
 }
 
 }  // namespace qsa

@@ -23,11 +23,11 @@
 //
 // Kernel layout: one persistent CTA per SM owns a contiguous range of
 // (token tile, cell tile) pairs and runs it as a warp-specialised pipeline:
-// two producer warps convert int8 codes to fp16 into a ring of four A stages
+// four producer warps convert int8 codes to fp16 into a ring of three A stages
 // (and copy qbar hi/lo into one of two B buffers when the token tile
 // changes), one thread issues the tcgen05 MMAs into one of two accumulator
 // sets in tensor memory (2 x 4 groups x 64 columns = 512 columns), and four
-// epilogue warps drain the other set to global memory.  Operands use the
+// eight epilogue warps drain the other set to global memory.  Operands use the
 // 128-byte-swizzled K-major layout read through shared-memory descriptors.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // QSA_DEVERR_TIMEOUT, all roles stop, tensor memory is freed and the kernel
@@ -49,10 +49,11 @@ constexpr int D = 128;
 constexpr int NG = 4;        // 32-dim scale groups
 constexpr int TM = 128;      // cells per tile (MMA M)
 constexpr int TN = 64;       // tokens per tile (MMA N)
-constexpr int NEPI = 4;      // epilogue warps 0..3
-constexpr int NPROD = 2;     // producer warps 4..5
-constexpr int MMA_WARP = 6;  // TMEM owner / MMA issuer
-constexpr int THREADS = 32 * 7;
+constexpr int NEPI = 8;      // epilogue warps 0..7 (TMEM lane quarter w % 4, token half w / 4)
+constexpr int NPROD = 4;     // producer warps 8..11
+constexpr int MMA_WARP = 12; // TMEM owner / MMA issuer
+constexpr int THREADS = 32 * 13;
+constexpr int PT = NPROD * 32;  // producer threads
 constexpr int NA = 3;        // A stages
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_BYTES = TM * D * 2;        // fp16, two 64-wide K blocks
@@ -203,7 +204,11 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
     return d;
 }
 
-__device__ __forceinline__ void named_sync_epilogue() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void named_sync_epilogue() { asm volatile("bar.sync 1, %0;" ::"n"(NEPI * 32) : "memory"); }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
+}
 
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, uint32_t src) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
@@ -239,10 +244,11 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
     return false;
 }
 
-// Warp roles: warps 0-3 drain the accumulators (epilogue; warp w owns TMEM
-// lanes 32w..32w+31, i.e. cells 32w.. of the tile), warps 4-5 produce the
-// operands (int8 codes -> fp16 A stages, qbar hi/lo -> B buffers), warp 6
-// allocates tensor memory and one of its threads issues the MMAs.  Stages
+// Warp roles: warps 0-7 drain the accumulators (epilogue; warp w owns TMEM
+// lanes 32(w%4).. i.e. cells 32(w%4).. of the tile, and token columns
+// 32(w/4)..+31), warps 8-11 produce the operands (int8 codes -> fp16 A
+// stages, qbar hi/lo -> B buffers by cp.async), warp 12 allocates tensor
+// memory and one of its threads issues the MMAs.  Stages
 // are handed over with mbarriers: a_full / a_empty (NA A stages), b_full /
 // b_empty (2 B buffers, one per token tile in flight), acc_full / acc_empty
 // (2 TMEM accumulator sets).
@@ -261,11 +267,11 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
 
     if (tid == 0) {
         for (int i = 0; i < NA; ++i) {
-            mbar_init(a_full + 8 * i, NPROD * 32);
+            mbar_init(a_full + 8 * i, PT);
             mbar_init(a_empty + 8 * i, 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(b_full + 8 * i, NPROD * 32);
+            mbar_init(b_full + 8 * i, PT);  // one cp.async-tracked arrival per producer thread
             mbar_init(b_empty + 8 * i, 1);
             mbar_init(acc_full + 8 * i, 1);
             mbar_init(acc_empty + 8 * i, NEPI * 32);
@@ -307,11 +313,11 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
         const int pt = tid - NEPI * 32;
         Walker w = w0;
         int nb = 0, cur_tt = -1;
-        uint4 pre[16];
+        uint4 pre[8];
         auto load_a = [&](int ct) {
 #pragma unroll
-            for (int it = 0; it < 16; ++it) {
-                const int q = it * (NPROD * 32) + pt, m = q >> 3, dc = q & 7;
+            for (int it = 0; it < 8; ++it) {
+                const int q = it * PT + pt, m = q >> 3, dc = q & 7;
                 const int c = ct * TM + m;
                 pre[it] = c < a.cache_cells ? __ldg(reinterpret_cast<const uint4 *>(a.kq + (size_t)c * D) + dc)
                                             : make_uint4(0u, 0u, 0u, 0u);
@@ -320,32 +326,22 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
         if (n > 0) load_a(w.ct);
         for (int k = 0; k < n; ++k) {
             if (w.tt != cur_tt) {
+                // qbar hi/lo rows of the new token tile: asynchronous copies
+                // into the swizzled B buffer, completing on b_full.
                 const int bs = nb & 1;
                 if (nb >= 2 && !mbar_wait_or_abort(b_empty + 8 * bs, ((nb >> 1) - 1) & 1, abort)) break;
                 const uint32_t dstB = sB + bs * B_PAIR;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint4 v[16];
-#pragma unroll
-                    for (int it = 0; it < 16; ++it) {
-                        const int q = (half * 16 + it) * (NPROD * 32) + pt, part = q >> 10, row = (q & 1023) >> 4,
-                                  ci = q & 15;
-                        v[it] = __ldg(reinterpret_cast<const uint4 *>(
-                                          a.qsum + ((size_t)(w.tt * TN + row) * 2 + part) * D) + ci);
-                    }
-#pragma unroll
-                    for (int it = 0; it < 16; ++it) {
-                        const int q = (half * 16 + it) * (NPROD * 32) + pt, part = q >> 10, row = (q & 1023) >> 4,
-                                  ci = q & 15;
-                        const int kb = ci >> 3, cc = ci & 7;
-                        const uint32_t p = dstB + part * B_BYTES + kb * B_KBLOCK + (row >> 3) * 1024 +
-                                           (row & 7) * 128 + ((cc ^ (row & 7)) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(p), "r"(v[it].x), "r"(v[it].y),
-                                     "r"(v[it].z), "r"(v[it].w));
-                    }
+                for (int it = 0; it < 2048 / PT; ++it) {
+                    const int q = it * PT + pt, part = q >> 10, row = (q & 1023) >> 4, ci = q & 15;
+                    const int kb = ci >> 3, cc = ci & 7;
+                    cp_async16(dstB + part * B_BYTES + kb * B_KBLOCK + (row >> 3) * 1024 + (row & 7) * 128 +
+                                   ((cc ^ (row & 7)) << 4),
+                               reinterpret_cast<const uint4 *>(a.qsum + ((size_t)(w.tt * TN + row) * 2 + part) * D) +
+                                   ci);
                 }
-                fence_async_smem();
-                mbar_arrive(b_full + 8 * bs);
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(b_full + 8 * bs)
+                             : "memory");
                 ++nb;
                 cur_tt = w.tt;
             }
@@ -353,8 +349,8 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
             if (k >= NA && !mbar_wait_or_abort(a_empty + 8 * st, ((k / NA) - 1) & 1, abort)) break;
             const uint32_t dstA = sA + st * A_BYTES;
 #pragma unroll
-            for (int it = 0; it < 16; ++it) {
-                const int q = it * (NPROD * 32) + pt, m = q >> 3, dc = q & 7;
+            for (int it = 0; it < 8; ++it) {
+                const int q = it * PT + pt, m = q >> 3, dc = q & 7;
                 uint32_t h[8];
                 codes_to_h2(pre[it].x ^ 0x80808080u, h[0], h[1]);
                 codes_to_h2(pre[it].y ^ 0x80808080u, h[2], h[3]);
@@ -373,6 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
             walk_next(a, w);
             if (k + 1 < n) load_a(w.ct);
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp == MMA_WARP) {
         // ---- MMA issuer ----
         if (lane == 0) {
@@ -424,7 +421,8 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
             const int b = k & 1;
             const int c0 = w.ct * TM, t0 = w.tt * TN;
             const bool full = use_tma && (c0 + TM - 1 <= a.pos0 + t0);
-            const int cell = c0 + warp * 32 + lane;
+            const int quarter = warp & 3, half = warp >> 2;
+            const int cell = c0 + quarter * 32 + lane;
             uint2 kv = make_uint2(0u, 0u);
             if (cell < a.cache_cells) kv = __ldg(reinterpret_cast<const uint2 *>(a.ksc + (size_t)cell * NG));
             if (!mbar_wait_or_abort(acc_full + 8 * b, (k >> 1) & 1, abort)) break;
@@ -440,11 +438,12 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
                 if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
                 named_sync_epilogue();
             }
-            const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * NG * TN);
+            const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NG * TN + half * (TN / 2));
             const int tmin = cell - a.pos0;  // first token whose causal range reaches `cell`
 #pragma unroll 1
-            for (int j0 = 0; j0 < TN; j0 += 16) {
-                if (!full && t0 + j0 >= a.ntok) break;  // warp-uniform
+            for (int j0 = 0; j0 < TN / 2; j0 += 16) {
+                const int tj = t0 + half * (TN / 2) + j0;  // first token of this 16-column chunk
+                if (!full && tj >= a.ntok) break;  // warp-uniform
                 uint32_t v[NG][16];
 #pragma unroll
                 for (int g = 0; g < NG; ++g) tmem_ld16(tbase + g * TN + j0, v[g]);
@@ -460,15 +459,15 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
                     o[j + 1] = __uint_as_float((uint32_t)(acc >> 32));
                 }
                 if (full) {
-                    const uint32_t dst = cbuf + (uint32_t)(j0 * TM + warp * 32 + lane) * 4;
+                    const uint32_t dst = cbuf + (uint32_t)((tj - t0) * TM + quarter * 32 + lane) * 4;
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + j * TM * 4), "f"(o[j]) : "memory");
                 } else {
-                    float *dst = a.scores + (size_t)(t0 + j0) * a.ld + cell;
+                    float *dst = a.scores + (size_t)tj * a.ld + cell;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const int t = t0 + j0 + j;
+                        const int t = tj + j;
                         if (t < a.ntok && t >= tmin) dst[(size_t)j * a.ld] = o[j];
                     }
                 }
