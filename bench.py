@@ -108,6 +108,27 @@ def traffic_record(kernel):
 
 
 # ---------------------------------------------------------------------------
+# multi-rank aggregation (one process per GPU; replicas, no data exchange)
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(x, device=None):
+    """The largest per-rank value (every rank gets it); x itself at world size 1."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(tokens_per_rank, world, slowest_ms):
+    """Whole-job tokens/s: every rank processes its own batch of
+    `tokens_per_rank` tokens; the job takes as long as the slowest rank."""
+    return world * tokens_per_rank / (slowest_ms / 1e3)
+
+
+# ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 
@@ -280,11 +301,7 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop()
     per = {n: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)] for i, n in enumerate(KERNELS)}
     step_ms = [evs[k][0].elapsed_time(evs[k][3]) for k in range(K)]
-    ms = sum(step_ms) / K
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(step_ms) / K, dev)
 
     # End to end through the public API: H2D of the step's inputs from pinned
     # host memory, the three calls, D2H of the attention output.
@@ -316,12 +333,8 @@ def run_ours(args, rank, world, local_rank):
             e1.record(stream)
             e1.synchronize()
             tot += e0.elapsed_time(e1)
-        e2e_ms = tot / K
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e_ms = max_over_ranks(tot / K, dev)
+        e2e = {"value": weak_scaling_value(T, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     # Roofline of the dominant kernel.
@@ -375,7 +388,7 @@ def main():
     cb = None
     if not args.no_cpu_baseline:
         cb = cpu_baseline(args.cpu_sample_seconds)
-    line = {"metric": METRIC, "value": world * args.ntok / (res["ms"] / 1e3), "unit": UNIT, "n_gpus": world,
+    line = {"metric": METRIC, "value": weak_scaling_value(args.ntok, world, res["ms"]), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "precision": "int8 K/V codes with fp16 scales; fp16 tensor-core operands, fp32 accumulation; "
