@@ -44,6 +44,11 @@ Pins (tests/test_oracle_pins.py):
                      softmax attention (torch scaled_dot_product_attention in
                      float64) for contiguous ids, chunked = unchunked softmax,
                      padding / permutation / duplication invariants.
+  select_ids      -- hand-built tiny rows (ranking by score, ties to the
+                     lower id, forced cells, causality), invariants on random
+                     rows (count, forced cells present, every selected free
+                     cell outranks every unselected one), and the special case
+                     of short contexts where every causal cell is selected.
 No function is left without a pin.
 """
 from __future__ import annotations
@@ -259,3 +264,43 @@ def attention(q: np.ndarray, kq, vq, ksc, vsc, ids: np.ndarray, softmax_scale: f
         O = (w[..., None] * o[nonempty]).sum(axis=0)
         out[r] = O / L[:, None]
     return out, out.astype(np.float16), part, bad
+
+
+# ---------------------------------------------------------------------------
+# Selection: scores -> ids  (argon_r36_qsa "Summary & Decision" buffer list:
+# scores, ids, pooled; sol_r5_mtp_qsa "mtp attention": the decode window of
+# 64 sink + 256 previous local + 1 current cell)
+# ---------------------------------------------------------------------------
+
+def select_ids(scores: np.ndarray, pos0: int, width: int = 2048, budget: int = 2048,
+               sink: int = 64, local: int = 256):
+    """Per token t (position p = pos0 + t), the ids its attention reads.
+
+    Reading (the pages name the scores -> ids step and its buffers but never
+    define it): the forced cells of the decode window -- sink cells
+    0 .. min(sink, p)-1, the previous `local` cells and the token's own cell
+    p -- plus the highest-scoring other causal cells c <= p, ties going to the
+    lower id, until min(p + 1, budget) cells are chosen; ascending, then -1 up
+    to `width`.  `scores` is [T, >= pos0 + T] (row t holds cells 0..p); the
+    decision is taken in the scores' own precision (float32).
+    """
+    T = scores.shape[0]
+    out = np.full((T, width), -1, dtype=np.int32)
+    for t in range(T):
+        p = pos0 + t
+        n = p + 1
+        k = min(n, budget)
+        forced = np.zeros(n, dtype=bool)
+        forced[: min(sink, n)] = True
+        forced[max(sink, p - local): p] = True
+        forced[p] = True
+        nf = int(forced.sum())
+        chosen = forced.copy()
+        if k > nf:
+            free = np.nonzero(~forced)[0]
+            s = scores[t, free].astype(np.float32)
+            order = np.lexsort((free, -s.astype(np.float64)))   # score descending, then id ascending
+            chosen[free[order[: k - nf]]] = True
+        ids = np.nonzero(chosen)[0]
+        out[t, : len(ids)] = ids
+    return out

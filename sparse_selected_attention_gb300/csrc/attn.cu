@@ -624,6 +624,12 @@ cudaError_t launch_attn(const AttnLaunch &a, cudaStream_t s) {
         attn_merge_kernel<<<a.ntok, D, 0, s>>>(a);
         return cudaGetLastError();
     }
+#ifndef QSA_ATTN_TC
+#define QSA_ATTN_TC 0
+#endif
+#if QSA_ATTN_TC
+    return launch_attn_tc(a, s);
+#endif
 #ifndef QSA_ATTN_NW
 #define QSA_ATTN_NW 4
 #endif

@@ -52,5 +52,8 @@ cudaError_t launch_score(const ScoreLaunch &a, cudaStream_t s);
 // a.qsum is ignored.  At most QSA_SCORE_NOALLOC_MAX_TOKENS tokens.
 cudaError_t launch_score_noalloc(const ScoreLaunch &a, cudaStream_t s);
 cudaError_t launch_attn(const AttnLaunch &a, cudaStream_t s);
+// Fused attention on tcgen05 (attn_tc.cu); same contract as the fused path of
+// launch_attn (part == NULL).
+cudaError_t launch_attn_tc(const AttnLaunch &a, cudaStream_t s);
 
 }  // namespace qsa

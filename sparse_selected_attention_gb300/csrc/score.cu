@@ -41,6 +41,7 @@
 
 #include "qsa.h"
 #include "qsa_internal.h"
+#include "tc_common.cuh"
 
 namespace qsa {
 namespace {
@@ -70,98 +71,15 @@ constexpr uint32_t SMEM_USED = OFF_FLAG + 16;
 // The layout needs more than half of an SM's shared memory, so exactly one
 // CTA (and one 512-column tensor-memory allocation) lives on each SM.
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
-constexpr long long WAIT_LIMIT = 1ll << 24;     // mbarrier polls before giving up
 
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory layout");
 
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
+using namespace tc;
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-    return r;
-}
-
-// 4 int8 codes (xor 0x80 applied) -> two packed fp16 pairs holding the exact
-// integers: 0x64xx is 1024 + xx, minus 1152 gives the signed code.
-__device__ __forceinline__ void codes_to_h2(uint32_t wx, uint32_t &lo, uint32_t &hi) {
-    const uint32_t m = 0x64646464u;
-    uint32_t a = prmt(wx, m, 0x4140), b = prmt(wx, m, 0x4342);
-    __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-    __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), bias);
-    __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
-    lo = *reinterpret_cast<uint32_t *>(&ha);
-    hi = *reinterpret_cast<uint32_t *>(&hb);
-}
-
-// --- tcgen05 / mbarrier wrappers --------------------------------------------
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait; returns false if the phase did not complete in time.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (long long i = 0; i < WAIT_LIMIT; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (stride byte offset); the leading byte offset is unused in
-// this mode; bits 46..48 hold the fixed value 0b001.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;
-    d |= (uint64_t)(1024u >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
-// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
-// (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bit 17,
-// M >> 4 at bit 24.
-constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
-
-__device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t acc) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
-        "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(acc));
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Instruction descriptor of the score tile: M = 128 cells, N = 64 tokens,
+// fp16 operands (both K-major), fp32 accumulation.
+constexpr uint32_t IDESC = idesc_f16(TM, TN, false, false);
 
 // --- kernels ----------------------------------------------------------------
 
@@ -230,20 +148,6 @@ __device__ __forceinline__ void walk_next(const ScoreLaunch &a, Walker &w) {
     }
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// Bounded wait that also gives up as soon as another role has given up.
-__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort) {
-    for (long long i = 0; i < WAIT_LIMIT; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255) == 255 && *abort) return false;
-    }
-    *abort = 1;
-    return false;
-}
-
 // Warp roles: warps 0-7 drain the accumulators (epilogue; warp w owns TMEM
 // lanes 32(w%4).. i.e. cells 32(w%4).. of the tile, and token columns
 // 32(w/4)..+31), warps 8-11 produce the operands (int8 codes -> fp16 A
@@ -279,15 +183,10 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == MMA_WARP) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32((const void *)tslot)),
-                     "r"(TMEM_COLS));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
-    tc_fence_before();
+    if (warp == MMA_WARP) tmem_alloc(smem_u32((const void *)tslot), TMEM_COLS);
+    fence_before();
     __syncthreads();
-    tc_fence_after();
+    fence_after();
     const uint32_t tmem = *tslot;
 
     // This CTA's contiguous share of the (token tile, cell tile) sequence.
@@ -385,23 +284,23 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
                 const int st = k % NA, b = k & 1;
                 if (!mbar_wait_or_abort(a_full + 8 * st, (k / NA) & 1, abort)) break;
                 if (k >= 2 && !mbar_wait_or_abort(acc_empty + 8 * b, ((k >> 1) - 1) & 1, abort)) break;
-                tc_fence_after();
-                const uint32_t aS = sA + st * A_BYTES, bS = sB + bs * B_PAIR;
+                fence_after();
+                const uint64_t ad0 = sw128_kmajor(sA + st * A_BYTES), bd0 = sw128_kmajor(sB + bs * B_PAIR);
 #pragma unroll
-                for (int g = 0; g < NG; ++g) {
-                    const uint32_t dt = tmem + (uint32_t)(b * NG * TN + g * TN);
+                for (int s2 = 0; s2 < 2; ++s2)
 #pragma unroll
-                    for (int s2 = 0; s2 < 2; ++s2) {
-                        const int ksx = 2 * g + s2, kb = ksx >> 2;
-                        const uint32_t koff = (ksx & 3) * 32;
-                        const uint64_t ad = sw128_desc(aS + kb * A_KBLOCK + koff);
+                    for (int part = 0; part < 2; ++part)
 #pragma unroll
-                        for (int part = 0; part < 2; ++part) {
-                            const uint64_t bd = sw128_desc(bS + part * B_BYTES + kb * B_KBLOCK + koff);
-                            mma_f16(dt, ad, bd, (s2 | part) ? 1u : 0u);
+                        for (int g = 0; g < NG; ++g) {
+                            // Groups innermost: consecutive MMAs target different
+                            // accumulators; only the descriptors' address field moves.
+                            const int ksx = 2 * g + s2, kb = ksx >> 2;
+                            const uint32_t koff = (ksx & 3) * 32;
+                            const uint32_t dt = tmem + (uint32_t)(b * NG * TN + g * TN);
+                            mma_f16(dt, ad0 + (uint64_t)((kb * A_KBLOCK + koff) >> 4),
+                                    bd0 + (uint64_t)((part * B_BYTES + kb * B_KBLOCK + koff) >> 4), IDESC,
+                                    (s2 | part) ? 1u : 0u);
                         }
-                    }
-                }
                 mma_commit(a_empty + 8 * st);
                 mma_commit(acc_full + 8 * b);
                 Walker nx = w;
@@ -426,7 +325,7 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
             uint2 kv = make_uint2(0u, 0u);
             if (cell < a.cache_cells) kv = __ldg(reinterpret_cast<const uint2 *>(a.ksc + (size_t)cell * NG));
             if (!mbar_wait_or_abort(acc_full + 8 * b, (k >> 1) & 1, abort)) break;
-            tc_fence_after();
+            fence_after();
             const float ks0 = __half2float(__ushort_as_half((unsigned short)(kv.x & 0xFFFF)));
             const float ks1 = __half2float(__ushort_as_half((unsigned short)(kv.x >> 16)));
             const float ks2 = __half2float(__ushort_as_half((unsigned short)(kv.y & 0xFFFF)));
@@ -472,7 +371,7 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
                     }
                 }
             }
-            tc_fence_before();
+            fence_before();
             mbar_arrive(acc_empty + 8 * b);
             if (full) {
                 fence_async_smem();
@@ -485,12 +384,12 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
         if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
 
-    tc_fence_before();
+    fence_before();
     __syncthreads();
     if (tid == 0 && *abort && a.err) atomicOr(a.err, QSA_DEVERR_TIMEOUT);
     if (warp == MMA_WARP) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+        fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 

@@ -306,3 +306,47 @@ def test_attention_part_and_empty_and_bad_ids():
     assert np.all(part[0, 1, :, 128] == -np.inf) and np.all(part[0, 1, :, 129] == 0)
     _, vv = _dequant(cache)
     np.testing.assert_array_equal(out64[2], np.broadcast_to(vv[3], (12, 128)))
+
+
+# ----------------------------------------------------------------------------
+# selection
+# ----------------------------------------------------------------------------
+
+from oracle import select_ids  # noqa: E402
+
+
+def test_select_short_context_takes_every_causal_cell():
+    sc = wl.uniform(3, 9, (5, 2100), -1, 1).astype(np.float32)
+    ids = select_ids(sc, pos0=10, width=2048)
+    for t in range(5):
+        p = 10 + t
+        assert np.array_equal(ids[t, : p + 1], np.arange(p + 1)) and np.all(ids[t, p + 1:] == -1)
+
+
+def test_select_hand_built_row():
+    # budget 6 with sink 2 and local 1: p = 9 forces {0, 1, 8, 9}; the two free
+    # slots go to the best of cells 2..7 by score, ties to the lower id.
+    sc = np.zeros((1, 10), dtype=np.float32)
+    sc[0, 2:8] = [0.5, 3.0, 3.0, -1.0, 3.0, 2.0]     # cells 3, 4, 6 tie at 3.0
+    sc[0, 8] = -100.0                                # forced cells ignore their score
+    ids = select_ids(sc, pos0=9, width=8, budget=6, sink=2, local=1)
+    assert ids[0].tolist() == [0, 1, 3, 4, 8, 9, -1, -1]
+
+
+def test_select_invariants_random():
+    T, pos0 = 9, 3000
+    sc = wl.normal(4, 10, (T, pos0 + T)).astype(np.float32)
+    sc[:, ::97] = 1.5                                # plenty of ties
+    ids = select_ids(sc, pos0, width=2048)
+    for t in range(T):
+        p = pos0 + t
+        row = ids[t][ids[t] >= 0]
+        assert len(row) == 2048 and np.all(np.diff(row) > 0) and row[-1] == p and row.max() <= p
+        forced = set(range(64)) | set(range(p - 256, p + 1))
+        assert forced <= set(row.tolist())
+        free_sel = np.array(sorted(set(row.tolist()) - forced))
+        unsel = np.array(sorted(set(range(p + 1)) - set(row.tolist())))
+        # every selected free cell outranks every unselected cell
+        worst = min(free_sel, key=lambda c: (sc[t, c], -c))
+        best_out = max(unsel, key=lambda c: (sc[t, c], -c))
+        assert (sc[t, worst], -worst) > (sc[t, best_out], -best_out)
