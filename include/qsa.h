@@ -187,6 +187,34 @@ typedef struct {
 #define QSA_SCORE_NOALLOC_MAX_TOKENS 8192
 qsa_status qsa_score_noalloc(const qsa_score_args *args, void *stream);
 
+/*
+ * qsa_select -- the scores -> ids step between qsa_score and qsa_attn.  The
+ * pages name its buffers ("Round 36 Track C ...", section "Summary &
+ * Decision": scores, ids, pooled) and the decode window ("round 5 track b:
+ * cached residual norms and fused mtp attention", section "mtp attention":
+ * 64 sink + 256 previous local + 1 current cell) but not the rule; this is
+ * the plainest reading.  For token t (p = pos0 + t):
+ *   forced = {0 .. min(sink, p+1)-1} U {max(sink, p-local) .. p-1} U {p};
+ *   the other causal cells c <= p are ranked by scores[t*ld + c] (float32,
+ *   descending; equal scores rank the lower id first) and the best
+ *   min(p+1, budget) - |forced| of them are added;
+ *   ids[t, :] = the chosen cells ascending, then -1 up to width.
+ * Deterministic and bit-exact for a given score array.
+ * scores [ntok, ld] fp32 (only c <= p read); ids [ntok, width] int32.
+ * Requires budget <= width, width % 64 == 0, pos0 + ntok <= ld and
+ * pos0 + ntok <= QSA_SELECT_MAX_CELLS (one row's scores are held on chip).
+ * scores 4-byte aligned, ids 4-byte aligned.
+ */
+#define QSA_SELECT_MAX_CELLS 32768
+typedef struct {
+    int ntok, pos0, width, budget, sink, local;
+    const float *scores;
+    int64_t ld;
+    int32_t *ids;
+} qsa_select_args;
+
+qsa_status qsa_select(const qsa_select_args *args, void *stream);
+
 qsa_status qsa_prep(const qsa_prep_args *args, void *stream);
 qsa_status qsa_score(const qsa_score_args *args, void *stream);
 qsa_status qsa_attn(const qsa_attn_args *args, void *stream);

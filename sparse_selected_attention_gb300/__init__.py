@@ -7,6 +7,7 @@ are rejected rather than computed elsewhere.
 
     qsa_prep   query RMS-norm + RoPE, K/V int8 quantisation into the cache
     qsa_score  head-reduced fp32 scores of every causal cache cell
+    qsa_select per-token selected cell ids from the scores
     qsa_attn   chunked attention over per-token selected cell ids
 """
 from __future__ import annotations
@@ -17,7 +18,7 @@ import math
 from . import _abi
 from ._abi import (QSA_DEVERR_BAD_ID, QSA_DEVERR_TIMEOUT, QSAError, lib)  # noqa: F401
 
-__all__ = ["qsa_prep", "qsa_score", "qsa_score_noalloc", "qsa_attn", "qsa_score_workspace_bytes", "qsa_abi_version",
+__all__ = ["qsa_prep", "qsa_score", "qsa_score_noalloc", "qsa_select", "qsa_attn", "qsa_score_workspace_bytes", "qsa_abi_version",
            "QSAError", "QSA_DEVERR_BAD_ID", "QSA_DEVERR_TIMEOUT", "lib"]
 
 
@@ -105,6 +106,20 @@ def qsa_score_noalloc(q, kq, ksc, pos0, scores, err=None, stream=None):
                        scores=_ptr(scores, "scores", torch.float32), ld=scores.shape[1],
                        workspace=None, workspace_bytes=0, err=_ptr(err, "err", torch.int32, optional=True))
     _abi.check(lib().qsa_score_noalloc(ctypes.byref(a), _stream(stream)))
+
+
+def qsa_select(scores, pos0, ids, budget=2048, sink=64, local=256, stream=None):
+    """ids [T, W] int32 <- the forced decode window plus the top-scoring causal
+    cells of each row of scores [T, ld] fp32 (ties to the lower id), ascending,
+    -1 padded."""
+    import torch
+    T = ids.shape[0]
+    if scores.dim() != 2 or scores.shape[0] < T:
+        raise ValueError("scores must be [T, ld]")
+    a = _abi.SelectArgs(ntok=T, pos0=int(pos0), width=ids.shape[1], budget=int(budget), sink=int(sink),
+                        local=int(local), scores=_ptr(scores, "scores", torch.float32), ld=scores.shape[1],
+                        ids=_ptr(ids, "ids", torch.int32))
+    _abi.check(lib().qsa_select(ctypes.byref(a), _stream(stream)))
 
 
 def qsa_attn(q, kq, vq, ksc, vsc, ids, out, softmax_scale=None, part=None, err=None, stream=None):

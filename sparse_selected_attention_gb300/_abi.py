@@ -17,6 +17,7 @@ QSA_OK, QSA_ERR_INVALID_ARG, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3
 QSA_DEVERR_BAD_ID, QSA_DEVERR_TIMEOUT = 1, 2
 QSA_F32, QSA_F16 = 0, 1
 QSA_SCORE_NOALLOC_MAX_TOKENS = 8192
+QSA_SELECT_MAX_CELLS = 32768
 
 _c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
 
@@ -34,6 +35,11 @@ class ScoreArgs(ctypes.Structure):
                 ("group", _c_int), ("cache_cells", _c_int),
                 ("q", _vp), ("q_dtype", _c_int), ("kq", _vp), ("ksc", _vp), ("scores", _vp),
                 ("ld", ctypes.c_int64), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("err", _vp)]
+
+
+class SelectArgs(ctypes.Structure):
+    _fields_ = [("ntok", _c_int), ("pos0", _c_int), ("width", _c_int), ("budget", _c_int), ("sink", _c_int),
+                ("local", _c_int), ("scores", _vp), ("ld", ctypes.c_int64), ("ids", _vp)]
 
 
 class AttnArgs(ctypes.Structure):
@@ -62,7 +68,7 @@ def lib() -> ctypes.CDLL:
                 "(the QSA path has no fallback)")
         L = ctypes.CDLL(LIB_PATH)
         for name, argt in (("qsa_prep", PrepArgs), ("qsa_score", ScoreArgs), ("qsa_attn", AttnArgs),
-                           ("qsa_score_noalloc", ScoreArgs)):
+                           ("qsa_score_noalloc", ScoreArgs), ("qsa_select", SelectArgs)):
             f = getattr(L, name)
             f.argtypes = [ctypes.POINTER(argt), _vp]
             f.restype = _c_int

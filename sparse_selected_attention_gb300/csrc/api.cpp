@@ -143,6 +143,26 @@ qsa_status qsa_attn(const qsa_attn_args *a, void *stream) {
     return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_attn");
 }
 
+qsa_status qsa_select(const qsa_select_args *a, void *stream) {
+    g_last_error[0] = 0;
+    if (!a) return fail(QSA_ERR_INVALID_ARG, "qsa_select: args is NULL");
+    if (a->ntok < 0 || a->pos0 < 0 || a->sink < 0 || a->local < 0 || a->budget < 1)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_select: negative ntok/pos0/sink/local or budget < 1");
+    if (a->width <= 0 || a->width % 64 != 0 || a->budget > a->width)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_select: width must be a positive multiple of 64 and >= budget");
+    if (a->ld < (long long)a->pos0 + a->ntok) return fail(QSA_ERR_INVALID_ARG, "qsa_select: ld < pos0 + ntok");
+    if ((long long)a->pos0 + a->ntok > QSA_SELECT_MAX_CELLS)
+        return fail(QSA_ERR_UNSUPPORTED, "qsa_select: rows longer than QSA_SELECT_MAX_CELLS cells");
+    if ((long long)a->sink + a->local + 1 > a->width)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_select: the forced window (sink + local + 1) exceeds width");
+    if (a->ntok == 0) return QSA_OK;
+    if (!a->scores || !a->ids) return fail(QSA_ERR_INVALID_ARG, "qsa_select: NULL buffer");
+    if (!aligned(a->scores, 4) || !aligned(a->ids, 4)) return fail(QSA_ERR_INVALID_ARG, "qsa_select: misaligned buffer");
+    qsa::SelectLaunch L{a->ntok, a->pos0, a->width, a->budget, a->sink, a->local, a->scores, a->ld, a->ids};
+    cudaError_t e = qsa::launch_select(L, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_select");
+}
+
 // Allocation-free scoring: same checks as qsa_score minus the workspace, plus
 // the built-in scratch limit.
 qsa_status qsa_score_noalloc(const qsa_score_args *a, void *stream) {

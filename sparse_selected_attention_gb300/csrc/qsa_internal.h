@@ -43,6 +43,16 @@ struct AttnLaunch {
     unsigned int *err;
 };
 
+struct SelectLaunch {
+    int ntok, pos0, width, budget, sink, local;
+    const float *scores;
+    int64_t ld;
+    int32_t *ids;
+};
+
+// Longest score row (cells) the selection kernel holds on chip.
+constexpr int kSelectMaxCells = 32768;
+
 // Token rows of the score workspace are padded to this multiple.
 constexpr int kScoreTokTile = 64;
 
@@ -52,6 +62,7 @@ cudaError_t launch_score(const ScoreLaunch &a, cudaStream_t s);
 // a.qsum is ignored.  At most QSA_SCORE_NOALLOC_MAX_TOKENS tokens.
 cudaError_t launch_score_noalloc(const ScoreLaunch &a, cudaStream_t s);
 cudaError_t launch_attn(const AttnLaunch &a, cudaStream_t s);
+cudaError_t launch_select(const SelectLaunch &a, cudaStream_t s);
 // Fused attention on tcgen05 (attn_tc.cu); same contract as the fused path of
 // launch_attn (part == NULL).
 cudaError_t launch_attn_tc(const AttnLaunch &a, cudaStream_t s);

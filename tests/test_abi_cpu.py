@@ -122,3 +122,26 @@ def test_prep_rejects(L, kw, want):
 def test_null_args_pointer(L):
     for fn in ("qsa_prep", "qsa_score", "qsa_attn"):
         assert getattr(L, fn)(None, None) == _abi.QSA_ERR_INVALID_ARG
+
+
+def _select(**kw):
+    a = _abi.SelectArgs(ntok=8, pos0=3000, width=2048, budget=2048, sink=64, local=256, scores=FAKE, ld=3008,
+                        ids=FAKE)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(width=2000), _abi.QSA_ERR_INVALID_ARG),
+    (dict(budget=4096), _abi.QSA_ERR_INVALID_ARG),
+    (dict(budget=0), _abi.QSA_ERR_INVALID_ARG),
+    (dict(ld=3007), _abi.QSA_ERR_INVALID_ARG),
+    (dict(pos0=40000, ld=40008), _abi.QSA_ERR_UNSUPPORTED),
+    (dict(width=256, budget=256), _abi.QSA_ERR_INVALID_ARG),
+    (dict(ids=None), _abi.QSA_ERR_INVALID_ARG),
+    (dict(scores=FAKE + 2), _abi.QSA_ERR_INVALID_ARG),
+])
+def test_select_rejects(L, kw, want):
+    s, msg = _status(L, "qsa_select", _select(**kw))
+    assert s == want and msg.startswith("qsa_select")

@@ -350,3 +350,11 @@ def test_select_invariants_random():
         worst = min(free_sel, key=lambda c: (sc[t, c], -c))
         best_out = max(unsel, key=lambda c: (sc[t, c], -c))
         assert (sc[t, worst], -worst) > (sc[t, best_out], -best_out)
+
+
+def test_select_signed_zeros_tie():
+    # -0.0 and +0.0 are the same score: the lower id wins, whatever the sign.
+    sc = np.full((1, 8), -1.0, dtype=np.float32)
+    sc[0, 2], sc[0, 3], sc[0, 4] = 0.0, -0.0, 0.0
+    ids = select_ids(sc, pos0=7, width=8, budget=4, sink=1, local=0)
+    assert ids[0].tolist() == [0, 2, 3, 7, -1, -1, -1, -1]

@@ -1,0 +1,81 @@
+"""qsa_select on the GPU against the oracle's select_ids on the same fp32
+scores (the selection is decided in the scores' precision, so ids must match
+bit for bit), including heavy ties, short contexts and the pipeline
+score -> select -> attention."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention, select_ids
+from sparse_selected_attention_gb300 import (qsa_attn, qsa_score, qsa_score_workspace_bytes, qsa_select)
+from sparse_selected_attention_gb300 import workloads as wl
+from tests.gpu_helpers import assert_f16_close, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run(scores, pos0, width=2048, budget=2048, sink=64, local=256):
+    T = scores.shape[0]
+    ids = torch.full((T, width), -7, dtype=torch.int32, device="cuda")
+    qsa_select(dev(scores), pos0, ids, budget=budget, sink=sink, local=local)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy()
+
+
+@pytest.mark.parametrize("T,pos0", [(64, 30000), (300, 2000), (8, 31970)])
+def test_select_matches_oracle_random(cuda_device, T, pos0):
+    sc = wl.normal(70, 1, (T, pos0 + T)).astype(np.float32)
+    got = run(sc, pos0)
+    assert np.array_equal(got, select_ids(sc, pos0))
+
+
+def test_select_full_size_sampled_rows(cuda_device):
+    T, pos0 = 1984, 30000
+    sc = wl.normal(71, 1, (T, pos0 + T)).astype(np.float32)
+    got = run(sc, pos0)
+    rows = np.array([0, 1, 511, 512, 1000, 1983])
+    for t in rows:
+        want = select_ids(sc[t:t + 1], pos0 + t)[0]
+        assert np.array_equal(got[t], want), t
+
+
+def test_select_heavy_ties(cuda_device):
+    T, pos0 = 40, 6000
+    sc = np.round(wl.normal(72, 1, (T, pos0 + T)) * 2) / 2      # few distinct values
+    sc = sc.astype(np.float32)
+    sc[:, 100:3000] = 0.5                                          # a wide plateau
+    sc[:, 3000:3200:2] = -0.0                                      # signed zeros tie with +0
+    sc[:, 3001:3200:2] = 0.0
+    assert np.array_equal(run(sc, pos0), select_ids(sc, pos0))
+
+
+def test_select_short_rows_and_window_only(cuda_device):
+    sc = wl.normal(73, 1, (50, 2100)).astype(np.float32)
+    assert np.array_equal(run(sc, 100), select_ids(sc, 100))        # n <= budget: every cell
+    sc2 = wl.normal(74, 1, (6, 4100)).astype(np.float32)
+    got = run(sc2, 4094, width=384, budget=321)                       # forced window only
+    assert np.array_equal(got, select_ids(sc2, 4094, width=384, budget=321))
+
+
+def test_score_select_attention_pipeline(cuda_device):
+    T, pos0 = 96, 9000
+    C = pos0 + T
+    cache = wl.make_cache(C, seed=75)
+    q32 = wl.queries_f32(T, seed=75)
+    q16 = q32.astype(np.float16)
+    kq, vq, ksc, vsc = dev(cache.kq), dev(cache.vq), dev(cache.ksc), dev(cache.vsc)
+    scores = torch.empty((T, C), dtype=torch.float32, device="cuda")
+    ws = torch.empty(qsa_score_workspace_bytes(T), dtype=torch.uint8, device="cuda")
+    qsa_score(dev(q32), kq, ksc, pos0, scores, ws)
+    ids = torch.empty((T, 2048), dtype=torch.int32, device="cuda")
+    qsa_select(scores, pos0, ids)
+    out = torch.empty((T, 12, 128), dtype=torch.float16, device="cuda")
+    qsa_attn(dev(q16), kq, vq, ksc, vsc, ids, out)
+    torch.cuda.synchronize()
+    sc = scores.cpu().numpy()
+    ref_ids = select_ids(sc, pos0)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    o64, _, _, _ = attention(q16, cache.kq, cache.vq, cache.ksc, cache.vsc, ref_ids, 1 / math.sqrt(128))
+    assert_f16_close(out.cpu(), o64, "score -> select -> attention")
