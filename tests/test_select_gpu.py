@@ -79,3 +79,36 @@ def test_score_select_attention_pipeline(cuda_device):
     assert np.array_equal(ids.cpu().numpy(), ref_ids)
     o64, _, _, _ = attention(q16, cache.kq, cache.vq, cache.ksc, cache.vsc, ref_ids, 1 / math.sqrt(128))
     assert_f16_close(out.cpu(), o64, "score -> select -> attention")
+
+
+@pytest.mark.parametrize("kind", ["all_equal", "outlier", "inf_range", "tiny_range", "two_plateaus", "mid_plateau"])
+def test_select_degenerate_rows(cuda_device, kind):
+    """Rows whose scores crowd into few values: plateaus at and around the
+    threshold, extreme outliers and spans a few ulps wide."""
+    T, pos0 = 12, 5000
+    sc = wl.normal(76, 1, (T, pos0 + T)).astype(np.float32)
+    if kind == "all_equal":
+        sc[:] = 1.25
+    elif kind == "outlier":
+        sc[:, 777] = 3e38
+    elif kind == "inf_range":
+        sc[:, 777] = 3e38                    # max - min overflows fp32
+        sc[:, 1234] = -3e38
+    elif kind == "tiny_range":
+        sc = (1.0 + np.round(sc * 4) * np.float32(2 ** -23)).astype(np.float32)  # a handful of ulps apart
+    elif kind == "mid_plateau":
+        sc[:, 1000:1800] = np.float32(0.33)  # ~800 ties straddling the threshold
+    else:
+        sc[:, :] = -2.0
+        sc[:, 200:2500] = 7.0                # more cells at 7.0 than the budget leaves free
+    assert np.array_equal(run(sc, pos0), select_ids(sc, pos0))
+
+
+@pytest.mark.parametrize("sink,local,budget", [(64, 256, 2048), (0, 5, 1000), (3, 0, 777)])
+def test_select_misaligned_rows(cuda_device, sink, local, budget):
+    """An odd row stride puts row starts at every offset modulo 16 bytes."""
+    T, pos0 = 16, 7001
+    sc = wl.normal(77, 1, (T, pos0 + T)).astype(np.float32)
+    assert sc.shape[1] % 2 == 1
+    got = run(sc, pos0, budget=budget, sink=sink, local=local)
+    assert np.array_equal(got, select_ids(sc, pos0, budget=budget, sink=sink, local=local))
