@@ -7,10 +7,15 @@ selected ids per token (W = 2048).  The step normalises/rotates the queries
 and quantises the new K/V rows into the cache, scores every causal cell
 (fp32 queries, 61.5 M scores written) and runs the selected-id attention.
 
+With --select the step also runs qsa_select between the score and the
+attention: each token keeps 64 sink cells, the previous 256 cells and its own
+cell, plus the best-scoring other causal cells up to 2048, and the attention
+reads those ids instead of the evenly spaced ones.
+
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--select]
 """
 from __future__ import annotations
 
@@ -37,6 +42,10 @@ WORKLOAD = ("prompt attention long context: T=1984 query tokens, pos0=30000, int
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 KERNELS = ("prep", "score", "attn")
+KERNELS_SELECT = ("prep", "score", "select", "attn")
+WORKLOAD_SELECT = WORKLOAD.replace("2048 evenly spaced causal ids per token",
+                                   "2048 ids per token chosen by qsa_select (64 sink + 256 local + current + "
+                                   "top-scoring causal cells)").replace("+ qsa_attn", "+ qsa_select + qsa_attn")
 
 
 def parse():
@@ -47,6 +56,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--ntok", type=int, default=NTOK, help="fewer tokens: for small profiling captures only")
     p.add_argument("--pos0", type=int, default=POS0, help="another context length: for profiling captures only")
+    p.add_argument("--select", action="store_true",
+                   help="step = prep + score + select + attention on the selected ids")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-sample-seconds", type=float, default=15.0)
@@ -72,6 +83,14 @@ def score_bytes(ntok, pos0, cells):
     """fp32 q read, int8 codes + fp16 scales of every cell read, one fp32 score
     written per causal (token, cell) pair."""
     return ntok * HQ * D * 4 + cells * (D + 2 * (D // G)) + 4 * score_pairs(ntok, pos0)
+
+
+def select_bytes(ntok, pos0, sink=64, local=256):
+    """Algorithmic bytes of one qsa_select launch: each token's free causal
+    scores (after the sink, before the local run), read once as fp32, and its
+    W int32 ids written."""
+    free = sum(max(min(max(sink, p - local), p) - sink, 0) for p in range(pos0, pos0 + ntok))
+    return 4 * free + 4 * ntok * WIDTH
 
 
 def prep_bytes(ntok):
@@ -238,7 +257,8 @@ def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
 
-    from sparse_selected_attention_gb300 import (qsa_attn, qsa_prep, qsa_score, qsa_score_workspace_bytes)
+    from sparse_selected_attention_gb300 import (qsa_attn, qsa_prep, qsa_score, qsa_score_workspace_bytes,
+                                                 qsa_select)
     from sparse_selected_attention_gb300 import workloads as wl
 
     torch.cuda.set_device(local_rank)
@@ -263,18 +283,29 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    names = KERNELS_SELECT if args.select else KERNELS
+    nk = len(names)
+
     def step(ev=None):
+        i = 0
         if ev:
-            ev[0].record(stream)
+            ev[i].record(stream)
         qsa_prep(q_in, k_in, v_in, norm_w, pos0, kq, vq, ksc, vsc, q16, q_out_f32=q32)
+        i += 1
         if ev:
-            ev[1].record(stream)
+            ev[i].record(stream)
         qsa_score(q32, kq, ksc, pos0, scores, ws)
+        if args.select:
+            i += 1
+            if ev:
+                ev[i].record(stream)
+            qsa_select(scores, pos0, ids)
+        i += 1
         if ev:
-            ev[2].record(stream)
+            ev[i].record(stream)
         qsa_attn(q16, kq, vq, ksc, vsc, ids, out)
         if ev:
-            ev[3].record(stream)
+            ev[i + 1].record(stream)
 
     def barrier():
         if world > 1:
@@ -287,7 +318,7 @@ def run_ours(args, rank, world, local_rank):
     barrier()
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(K)]
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
@@ -299,8 +330,8 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
-    per = {n: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)] for i, n in enumerate(KERNELS)}
-    step_ms = [evs[k][0].elapsed_time(evs[k][3]) for k in range(K)]
+    per = {n: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)] for i, n in enumerate(names)}
+    step_ms = [evs[k][0].elapsed_time(evs[k][nk]) for k in range(K)]
     ms = max_over_ranks(sum(step_ms) / K, dev)
 
     # End to end through the public API: H2D of the step's inputs from pinned
@@ -310,7 +341,8 @@ def run_ours(args, rank, world, local_rank):
         h_q, h_k, h_v = (torch.from_numpy(x).pin_memory() for x in (inp.q_in, inp.k_in, inp.v_in))
         h_ids = torch.from_numpy(ids_np).pin_memory()
         h_out = torch.empty((T, HQ, D), dtype=torch.float16).pin_memory()
-        h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_ids))
+        h_in = (h_q, h_k, h_v) if args.select else (h_q, h_k, h_v, h_ids)  # selected ids are made on the device
+        h2d = sum(x.numel() * x.element_size() for x in h_in)
         d2h = h_out.numel() * h_out.element_size()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -318,7 +350,8 @@ def run_ours(args, rank, world, local_rank):
             q_in.copy_(h_q, non_blocking=True)
             k_in.copy_(h_k, non_blocking=True)
             v_in.copy_(h_v, non_blocking=True)
-            ids.copy_(h_ids, non_blocking=True)
+            if not args.select:
+                ids.copy_(h_ids, non_blocking=True)
             step()
             h_out.copy_(out, non_blocking=True)
 
@@ -340,21 +373,22 @@ def run_ours(args, rank, world, local_rank):
     # Roofline of the dominant kernel.
     avg = {n: sum(v) / K for n, v in per.items()}
     dom = max(avg, key=avg.get)
-    ab, valid = attn_bytes(ids_np, T)
+    ab, valid = attn_bytes(ids.cpu().numpy() if args.select else ids_np, T)
     alg = {"attn": ab, "score": score_bytes(T, pos0, C), "prep": prep_bytes(T)}
+    if args.select:
+        alg["select"] = select_bytes(T, pos0)
     peak, peak_src = peaks()
     achieved = alg[dom] / (avg[dom] / 1e3) / 1e9
-    src = {"attn": "attn.cu", "score": "score.cu", "prep": "prep.cu"}[dom]
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": traffic_record(dom), "kernel": dom, "peak_source": peak_src,
             "algorithmic_bytes_per_launch": alg[dom], "avg_launch_ms": avg[dom]}
     kernels = {n: {"avg_ms": avg[n], "algorithmic_bytes": alg[n],
-                   "achieved_gbs": alg[n] / (avg[n] / 1e3) / 1e9} for n in KERNELS}
+                   "achieved_gbs": alg[n] / (avg[n] / 1e3) / 1e9} for n in names}
     kernels["score"]["pairs"] = score_pairs(T, pos0)
     kernels["score"]["tflops_algorithmic"] = 2 * HQ * D * score_pairs(T, pos0) / (avg["score"] / 1e3) / 1e12
     kernels["attn"]["valid_cells"] = valid
     return {"ms": ms, "wall_s": wall, "e2e": e2e, "clocks": clocks, "roofline": roof, "kernels": kernels,
-            "launches_per_step": 4}
+            "launches_per_step": 5 if args.select else 4}
 
 
 def main():
@@ -362,7 +396,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    config = {"workload": WORKLOAD, "ntok": args.ntok, "pos0": args.pos0, "cache_cells": args.pos0 + args.ntok,
+    config = {"workload": WORKLOAD_SELECT if args.select else WORKLOAD, "ntok": args.ntok, "pos0": args.pos0, "cache_cells": args.pos0 + args.ntok,
               "width": WIDTH, "heads": "12 query / 1 KV", "head_dim": D,
               "l2": "flushed between steps (256 MiB write), flush outside the step events",
               "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
