@@ -202,25 +202,39 @@ CHUNK = 64
 
 
 def attention(q: np.ndarray, kq, vq, ksc, vsc, ids: np.ndarray, softmax_scale: float,
-              rows=None, group: int = 32, want_part: bool = False):
+              rows=None, group: int = 32, want_part: bool = False, gate=None):
     """Chunked attention over each token's selected cells, max-first merge.
 
     For token t and head h, chunk c holds id slots 64c .. 64c+63; J_c is the
     set of slots with a valid id (0 <= id < cells; -1 and out-of-range ids
-    are padding and contribute nothing).
-      s_j  = scale * sum_g ksc[id,g] * sum_{d in g} q[t,h,d] * kq[id,d]
+    are padding and contribute nothing).  Head h reads KV head
+    kv = h // (H / Hkv) ("round 5 track b: cached residual norms and fused mtp
+    attention", section "mtp attention": a grid of 2 KV heads per token, 24
+    heads of partials, 12 query heads per KV row).  kq, vq are [cells, D] for
+    one KV head or [cells, Hkv, D]; ksc, vsc [cells, D/group] or
+    [cells, Hkv, D/group].
+      s_j  = scale * sum_g ksc[id,kv,g] * sum_{d in g} q[t,h,d] * kq[id,kv,d]
       m_c  = max_{j in J_c} s_j ;  p_j = exp(s_j - m_c) ;  l_c = sum p_j
-      o_c[d] = sum_j p_j * vsc[id, d // group] * vq[id, d]
+      o_c[d] = sum_j p_j * vsc[id, kv, d // group] * vq[id, kv, d]
     Empty chunks are skipped.  Merge (max-first):
-      M = max_c m_c ; L = sum_c exp(m_c - M) l_c ;
-      out = fp16_rne( sum_c exp(m_c - M) o_c / L )
+      M = max_c m_c ; L = sum_c exp(m_c - M) l_c ;  O = sum_c exp(m_c - M) o_c / L
+    Output gate (same section: "sigmoid gate", fp32 gates beside the fp32
+    queries), optional, one value per (t, h, d):
+      out = fp16_rne( O * 1 / (1 + exp(-gate[t,h,d])) )   (ungated: fp16_rne(O))
     A token with no valid id outputs +0.
 
     Returns (out float64 [R,H,D] before fp16 rounding, out fp16,
     part float64 [R, W/64, H, D+2] = (o_c, m_c, l_c) or None, bad_id flag).
+    The partials are the ungated chunk values.
     """
     q = np.asarray(q)
     T, H, D = q.shape
+    kq, vq, ksc, vsc = (np.asarray(x) for x in (kq, vq, ksc, vsc))
+    if kq.ndim == 2:                                       # one KV head
+        kq, vq, ksc, vsc = kq[:, None], vq[:, None], ksc[:, None], vsc[:, None]
+    Hkv = kq.shape[1]
+    assert H % Hkv == 0, "query heads must split evenly over the KV heads"
+    per = H // Hkv
     rows = np.arange(T) if rows is None else np.asarray(rows)
     C = kq.shape[0]
     W = ids.shape[1]
@@ -232,37 +246,41 @@ def attention(q: np.ndarray, kq, vq, ksc, vsc, ids: np.ndarray, softmax_scale: f
     kscale = ksc.astype(np.float64)
     vscale = vsc.astype(np.float64)
     for r, t in enumerate(rows):
-        qt = q[t].astype(np.float64)                       # [H, D]
         row = np.full(nch * CHUNK, -1, dtype=np.int64)
         row[:W] = ids[t]
         row = row.reshape(nch, CHUNK)
         valid = (row >= 0) & (row < C)
         safe = np.where(valid, row, 0)
-        k = kq[safe].astype(np.float64)                     # [nch, 64, D]
-        v = vq[safe].astype(np.float64)
-        s = np.zeros((nch, CHUNK, H), dtype=np.float64)
-        for g in range(ng):
-            sl = slice(g * group, (g + 1) * group)
-            s += kscale[safe][..., g:g + 1] * (k[..., sl] @ qt[:, sl].T)
-        s *= softmax_scale
-        s = np.where(valid[..., None], s, -np.inf)
         nonempty = valid.any(axis=1)                       # [nch]
-        m = np.where(nonempty[:, None], s.max(axis=1), -np.inf)     # [nch, H]
-        p = np.where(valid[..., None], np.exp(s - np.where(nonempty[:, None], m, 0.0)[:, None, :]), 0.0)
-        l = p.sum(axis=1)                                  # [nch, H]
-        vdq = v * np.repeat(vscale[safe], group, axis=-1)  # [nch, 64, D]
-        o = np.einsum("cjh,cjd->chd", p, vdq)              # [nch, H, D]
-        if want_part:
-            part[r, :, :, :D] = o
-            part[r, :, :, D] = m
-            part[r, :, :, D + 1] = l
-        if not nonempty.any():
-            continue
-        M = m[nonempty].max(axis=0)                        # [H]
-        w = np.exp(m[nonempty] - M[None, :])               # [nne, H]
-        L = (w * l[nonempty]).sum(axis=0)
-        O = (w[..., None] * o[nonempty]).sum(axis=0)
-        out[r] = O / L[:, None]
+        for kv in range(Hkv):
+            hs = slice(kv * per, (kv + 1) * per)
+            qt = q[t, hs].astype(np.float64)               # [per, D]
+            k = kq[safe, kv].astype(np.float64)            # [nch, 64, D]
+            v = vq[safe, kv].astype(np.float64)
+            s = np.zeros((nch, CHUNK, per), dtype=np.float64)
+            for g in range(ng):
+                sl = slice(g * group, (g + 1) * group)
+                s += kscale[safe, kv][..., g:g + 1] * (k[..., sl] @ qt[:, sl].T)
+            s *= softmax_scale
+            s = np.where(valid[..., None], s, -np.inf)
+            m = np.where(nonempty[:, None], s.max(axis=1), -np.inf)     # [nch, per]
+            p = np.where(valid[..., None], np.exp(s - np.where(nonempty[:, None], m, 0.0)[:, None, :]), 0.0)
+            l = p.sum(axis=1)                              # [nch, per]
+            vdq = v * np.repeat(vscale[safe, kv], group, axis=-1)       # [nch, 64, D]
+            o = np.einsum("cjh,cjd->chd", p, vdq)          # [nch, per, D]
+            if want_part:
+                part[r, :, hs, :D] = o
+                part[r, :, hs, D] = m
+                part[r, :, hs, D + 1] = l
+            if not nonempty.any():
+                continue
+            M = m[nonempty].max(axis=0)                    # [per]
+            w = np.exp(m[nonempty] - M[None, :])           # [nne, per]
+            L = (w * l[nonempty]).sum(axis=0)
+            O = (w[..., None] * o[nonempty]).sum(axis=0)
+            out[r, hs] = O / L[:, None]
+        if gate is not None:
+            out[r] *= 1.0 / (1.0 + np.exp(-np.asarray(gate[t], dtype=np.float64)))
     return out, out.astype(np.float16), part, bad
 
 

@@ -82,7 +82,7 @@ def int8_uniform(seed: int, stream: int, shape) -> np.ndarray:
 
 
 # Stream numbers: one per drawn tensor, so changing one shape leaves the others.
-_S_KQ, _S_VQ, _S_KSC, _S_VSC, _S_Q16, _S_Q32, _S_QIN, _S_KIN, _S_VIN, _S_G, _S_EDGE = range(1, 12)
+_S_KQ, _S_VQ, _S_KSC, _S_VSC, _S_Q16, _S_Q32, _S_QIN, _S_KIN, _S_VIN, _S_G, _S_EDGE, _S_GATE = range(1, 13)
 
 
 @dataclasses.dataclass
@@ -103,15 +103,33 @@ class Cache:
 
 
 def make_cache(cells: int, seed: int = 5, head_dim: int = HEAD_DIM, group: int = GROUP,
-               scale_lo: float = 1e-3, scale_hi: float = 2e-2) -> Cache:
-    """Cache of `cells` rows: codes uniform on [-127,127], scales fp16(U[lo,hi])."""
+               scale_lo: float = 1e-3, scale_hi: float = 2e-2, kv_heads: int = 1) -> Cache:
+    """Cache of `cells` rows: codes uniform on [-127,127], scales fp16(U[lo,hi]).
+    One KV head: kq/vq [cells, D], scales [cells, D/group]; more: kq/vq
+    [cells, kv_heads, D], scales [cells, kv_heads, D/group]."""
     ng = head_dim // group
+    row = (cells, head_dim) if kv_heads == 1 else (cells, kv_heads, head_dim)
+    srow = (cells, ng) if kv_heads == 1 else (cells, kv_heads, ng)
     return Cache(
-        kq=int8_uniform(seed, _S_KQ, (cells, head_dim)),
-        vq=int8_uniform(seed, _S_VQ, (cells, head_dim)),
-        ksc=uniform(seed, _S_KSC, (cells, ng), scale_lo, scale_hi).astype(np.float16),
-        vsc=uniform(seed, _S_VSC, (cells, ng), scale_lo, scale_hi).astype(np.float16),
+        kq=int8_uniform(seed, _S_KQ, row),
+        vq=int8_uniform(seed, _S_VQ, row),
+        ksc=uniform(seed, _S_KSC, srow, scale_lo, scale_hi).astype(np.float16),
+        vsc=uniform(seed, _S_VSC, srow, scale_lo, scale_hi).astype(np.float16),
     )
+
+
+# The pages' own attention shape ("round 5 track b: cached residual norms and
+# fused mtp attention", section "mtp attention": two KV heads per token, 24
+# heads of 256 + 2 partial floats, fp16 per-64 scales, seed 20260701) and
+# the matching softmax scale 1/sqrt(256).
+PAGES_KV_HEADS, PAGES_Q_HEADS, PAGES_HEAD_DIM, PAGES_GROUP = 2, 24, 256, 64
+PAGES_SCALE = 0.0625
+PAGES_SEED = 20260701
+
+
+def gates_f32(ntok: int, seed: int = 5, heads: int = N_Q_HEADS, head_dim: int = HEAD_DIM) -> np.ndarray:
+    """fp32 output-gate logits, 2 * N(0,1) (so some saturate). [ntok, heads, D]."""
+    return (2.0 * normal(seed, _S_GATE, (ntok, heads, head_dim))).astype(np.float32)
 
 
 def queries_f16(ntok: int, seed: int = 5, heads: int = N_Q_HEADS, head_dim: int = HEAD_DIM) -> np.ndarray:

@@ -358,3 +358,68 @@ def test_select_signed_zeros_tie():
     sc[0, 2], sc[0, 3], sc[0, 4] = 0.0, -0.0, 0.0
     ids = select_ids(sc, pos0=7, width=8, budget=4, sink=1, local=0)
     assert ids[0].tolist() == [0, 2, 3, 7, -1, -1, -1, -1]
+
+
+# ----------------------------------------------------------------------------
+# attention: output gate and several KV heads
+# ----------------------------------------------------------------------------
+
+def test_attention_gate_zero_halves_the_output_exactly():
+    cache = wl.make_cache(400, seed=31)
+    q = wl.queries_f16(3, seed=31)
+    ids = wl.even_ids(3, 390, width=256, select=256)
+    plain, _, _, _ = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, ids, SCALE)
+    gated, _, _, _ = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, ids, SCALE,
+                               gate=np.zeros((3, 12, 128), np.float32))
+    assert np.array_equal(gated, plain * 0.5)
+
+
+def test_attention_gate_applies_per_head_and_dim():
+    # sigmoid(ln 3) = 3/4 and sigmoid(-ln 3) = 1/4; the pattern varies along
+    # both the head and the dim axis, so a transposed or per-head gate fails.
+    cache = wl.make_cache(300, seed=32)
+    q = wl.queries_f16(2, seed=32)
+    ids = wl.even_ids(2, 290, width=128, select=128)
+    h, d = np.meshgrid(np.arange(12), np.arange(128), indexing="ij")
+    code = (h + 2 * d) % 3                                   # 0, 1, 2
+    gate = np.where(code == 0, 0.0, np.where(code == 1, np.log(3.0), -np.log(3.0)))
+    factor = np.where(code == 0, 0.5, np.where(code == 1, 0.75, 0.25))
+    plain, _, _, _ = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, ids, SCALE)
+    gated, _, _, _ = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, ids, SCALE,
+                               gate=np.broadcast_to(gate, (2, 12, 128)))
+    np.testing.assert_allclose(gated, plain * factor[None], rtol=1e-14, atol=0)
+
+
+def test_attention_two_kv_heads_equal_grouped_sdpa():
+    # The pages' shape: 2 KV heads, 12 query heads each, d = 256, per-64
+    # scales.  Contiguous causal ids reduce it to dense causal attention with
+    # grouped KV heads, which torch computes with enable_gqa.
+    T, pos0 = 20, 60
+    H, Hkv, D, grp = wl.PAGES_Q_HEADS, wl.PAGES_KV_HEADS, wl.PAGES_HEAD_DIM, wl.PAGES_GROUP
+    cache = wl.make_cache(pos0 + T, seed=33, head_dim=D, group=grp, kv_heads=Hkv)
+    q = wl.queries_f16(T, seed=33, heads=H, head_dim=D)
+    ids = wl.even_ids(T, pos0, width=128, select=4096)
+    out64, _, _, _ = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, ids, wl.PAGES_SCALE, group=grp)
+    k = cache.kq.astype(np.float64) * np.repeat(cache.ksc.astype(np.float64), grp, axis=-1)   # [C, Hkv, D]
+    v = cache.vq.astype(np.float64) * np.repeat(cache.vsc.astype(np.float64), grp, axis=-1)
+    Q = torch.from_numpy(q.astype(np.float64)).permute(1, 0, 2)[None]      # [1, H, T, D]
+    K = torch.from_numpy(k).permute(1, 0, 2)[None]                          # [1, Hkv, C, D]
+    V = torch.from_numpy(v).permute(1, 0, 2)[None]
+    mask = torch.arange(pos0 + T)[None, :] <= (pos0 + torch.arange(T))[:, None]
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=wl.PAGES_SCALE,
+                                                           enable_gqa=True)
+    np.testing.assert_allclose(out64, ref[0].permute(1, 0, 2).numpy(), rtol=1e-10, atol=1e-13)
+
+
+def test_attention_kv_head_slices_are_independent():
+    # Changing KV head 1's rows changes only query heads 12..23.
+    T, pos0, D, grp = 3, 200, 256, 64
+    cache = wl.make_cache(pos0 + T, seed=34, head_dim=D, group=grp, kv_heads=2)
+    q = wl.queries_f16(T, seed=34, heads=24, head_dim=D)
+    ids = wl.even_ids(T, pos0, width=128, select=128)
+    a, _, _, _ = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, ids, 0.0625, group=grp)
+    vq2 = cache.vq.copy()
+    vq2[:, 1] = -vq2[:, 1]
+    b, _, _, _ = attention(q, cache.kq, vq2, cache.ksc, cache.vsc, ids, 0.0625, group=grp)
+    assert np.array_equal(a[:, :12], b[:, :12])
+    np.testing.assert_allclose(b[:, 12:], -a[:, 12:], rtol=1e-12, atol=1e-15)
