@@ -58,6 +58,9 @@ def parse():
     p.add_argument("--pos0", type=int, default=POS0, help="another context length: for profiling captures only")
     p.add_argument("--select", action="store_true",
                    help="step = prep + score + select + attention on the selected ids")
+    p.add_argument("--pages-shape", action="store_true",
+                   help="time the attention alone at the pages' own shape (2 KV x 12 heads, head_dim 256, "
+                        "per-64 scales) on the same token / id workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-sample-seconds", type=float, default=15.0)
@@ -68,11 +71,12 @@ def parse():
 # algorithmic work per launch (bytes the method must move, flops it must do)
 # ---------------------------------------------------------------------------
 
-def attn_bytes(ids_np, ntok):
-    """Gathered bytes: per valid id 2 * (D + 2*D/G) = 272 B (K and V codes plus
-    scales), every id slot read (4 B), q read and out written (fp16)."""
+def attn_bytes(ids_np, ntok, hkv=1, hq=HQ, d=D):
+    """Gathered bytes: per valid id and KV head 2 * (d + 8) (K and V codes plus
+    four fp16 scales each; 272 B at d = 128), every id slot read (4 B), q read
+    and out written (fp16)."""
     valid = int((ids_np >= 0).sum())
-    return valid * 2 * (D + 2 * (D // G)) + ids_np.size * 4 + 2 * ntok * HQ * D * 2, valid
+    return valid * hkv * 2 * (d + 8) + ids_np.size * 4 + 2 * ntok * hq * d * 2, valid
 
 
 def score_pairs(ntok, pos0):
@@ -391,6 +395,61 @@ def run_ours(args, rank, world, local_rank):
             "launches_per_step": 5 if args.select else 4}
 
 
+def run_pages(args, rank, world, local_rank):
+    """The attention alone at the pages' shape: 2 KV heads x 12 query heads,
+    head_dim 256, per-64 scales, softmax scale 1/16, on the same tokens and
+    evenly spaced ids as the default step; L2 flushed between launches."""
+    import numpy as np
+    import torch
+
+    from sparse_selected_attention_gb300 import qsa_attn
+    from sparse_selected_attention_gb300 import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    T, pos0 = args.ntok, args.pos0
+    hq, hkv, d, grp = wl.PAGES_Q_HEADS, wl.PAGES_KV_HEADS, wl.PAGES_HEAD_DIM, wl.PAGES_GROUP
+    cache = wl.make_cache(pos0 + T, seed=wl.PAGES_SEED + rank, head_dim=d, group=grp, kv_heads=hkv)
+    ids_np = wl.even_ids(T, pos0, WIDTH)
+
+    def to(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+    kq, vq, ksc, vsc = to(cache.kq), to(cache.vq), to(cache.ksc), to(cache.vsc)
+    q = to(wl.queries_f16(T, seed=wl.PAGES_SEED + rank, heads=hq, head_dim=d))
+    ids = to(ids_np)
+    out = torch.empty((T, hq, d), dtype=torch.float16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.zero_()
+        qsa_attn(q, kq, vq, ksc, vsc, ids, out, wl.PAGES_SCALE)
+    torch.cuda.synchronize()
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for k in range(K):
+        flush.zero_()
+        evs[k][0].record(stream)
+        qsa_attn(q, kq, vq, ksc, vsc, ids, out, wl.PAGES_SCALE)
+        evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / K, dev)
+    ab, valid = attn_bytes(ids_np, T, hkv=hkv, hq=hq, d=d)
+    peak, peak_src = peaks()
+    achieved = ab / (ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": None, "kernel": "attn (pages' shape)", "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": ab, "avg_launch_ms": ms}
+    return {"ms": ms, "clocks": clocks, "roofline": roof, "valid_cells": valid}
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -416,6 +475,22 @@ def main():
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if args.pages_shape:
+        res = run_pages(args, rank, world, local_rank)
+        if rank == 0:
+            config["workload"] = ("attention alone at the pages' shape: T=%d query tokens at pos0=%d, 2 KV heads x "
+                                  "12 query heads, head_dim 256, fp16 per-64 scales, softmax scale 1/16, int8 K/V "
+                                  "cache of %d cells, %d evenly spaced causal ids per token"
+                                  % (args.ntok, args.pos0, args.pos0 + args.ntok, WIDTH))
+            config["heads"] = "24 query / 2 KV"
+            config["head_dim"] = 256
+            line = {"metric": METRIC, "value": weak_scaling_value(args.ntok, world, res["ms"]), "unit": UNIT,
+                    "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+                    "data": "synthetic", "config": config, "roofline": res["roofline"], "clocks": res["clocks"],
+                    "gpu_launches": args.steps, "valid_cells": res["valid_cells"]}
+            print(json.dumps(line), flush=True)
+        return
     res = run_ours(args, rank, world, local_rank)
     if rank != 0:
         return

@@ -35,7 +35,7 @@
 extern "C" {
 #endif
 
-#define QSA_ABI_VERSION 1
+#define QSA_ABI_VERSION 2
 
 typedef enum {
     QSA_OK = 0,
@@ -131,22 +131,31 @@ size_t qsa_score_workspace_bytes(int ntok, int head_dim);
  *
  * For token t and head h, chunk c covers id slots 64c .. 64c+63; a slot is
  * valid when 0 <= id < cache_cells (ids < -1 or >= cache_cells are treated
- * as padding and set QSA_DEVERR_BAD_ID).
- *   s_j = softmax_scale * sum_g ksc[id,g] * sum_{d in g} q[t,h,d] * kq[id,d]
+ * as padding and set QSA_DEVERR_BAD_ID).  Head h reads KV head
+ * kv = h / (n_q_heads / n_kv_heads) (the pages' mtp grid: two KV heads per
+ * token, 12 query heads on each).
+ *   s_j = softmax_scale * sum_g ksc[id,kv,g] * sum_{d in g} q[t,h,d] * kq[id,kv,d]
  *   m_c = max s_j, l_c = sum exp(s_j - m_c), o_c = sum exp(s_j - m_c) v_j
- *   with v_j[d] = vsc[id, d/group] * vq[id, d];
- *   out = fp16(sum_c exp(m_c - M) o_c / sum_c exp(m_c - M) l_c), M = max m_c.
+ *   with v_j[d] = vsc[id, kv, d/group] * vq[id, kv, d];
+ *   O = sum_c exp(m_c - M) o_c / sum_c exp(m_c - M) l_c, M = max m_c;
+ *   out = fp16(O), or with a gate (same section: "sigmoid gate", fp32 gates)
+ *   out[t,h,d] = fp16(O[t,h,d] / (1 + exp(-gate[t,h,d]))).
  * A token with no valid slot outputs +0.
  *
- * q [ntok, n_q_heads, head_dim] fp16; ids [ntok, width] int32, width a
- * multiple of 64; out [ntok, n_q_heads, head_dim] fp16.
+ * q [ntok, n_q_heads, head_dim] fp16; kq, vq [cache_cells, n_kv_heads,
+ * head_dim] int8; ksc, vsc [cache_cells, n_kv_heads, head_dim/group] fp16;
+ * ids [ntok, width] int32, width a multiple of 64; out [ntok, n_q_heads,
+ * head_dim] fp16; gate NULL or [ntok, n_q_heads, head_dim] fp32.
  * part: NULL, or [ntok, width/64, n_q_heads, head_dim + 2] fp32 receiving each
- * chunk's (o_c[0..head_dim), m_c, l_c); an empty chunk gives (0, -inf, 0).
- * A non-NULL part selects the split path (per-chunk kernel, then a merge
- * kernel that reads part back); NULL selects the fused single-kernel path.
- * Supported: n_kv_heads == 1, head_dim == 128, group == 32,
- * 1 <= n_q_heads <= 16.  q, kq, vq, out, part 16-byte aligned; ksc, vsc
- * 8-byte; ids 4-byte.
+ * chunk's ungated (o_c[0..head_dim), m_c, l_c); an empty chunk gives
+ * (0, -inf, 0).  A non-NULL part selects the split path (per-chunk kernel,
+ * then a merge kernel that reads part back); NULL selects the fused
+ * single-kernel path.  All pointers are device pointers owned by the caller.
+ * Supported: (head_dim 128, group 32) -- the workload's shape -- or
+ * (head_dim 256, group 64) -- the pages' own; n_q_heads a multiple of
+ * n_kv_heads with 1..16 query heads per KV head; otherwise
+ * QSA_ERR_UNSUPPORTED.  q, kq, vq, out, part 16-byte aligned; ksc, vsc
+ * 8-byte; ids, gate 4-byte.
  */
 typedef struct {
     int ntok, n_q_heads, n_kv_heads, head_dim, group, cache_cells, width;
@@ -158,6 +167,7 @@ typedef struct {
     uint16_t *out;
     float *part;
     unsigned int *err;
+    const float *gate; /* added in ABI version 2 */
 } qsa_attn_args;
 
 /*

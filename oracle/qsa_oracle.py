@@ -280,7 +280,8 @@ def attention(q: np.ndarray, kq, vq, ksc, vsc, ids: np.ndarray, softmax_scale: f
             O = (w[..., None] * o[nonempty]).sum(axis=0)
             out[r, hs] = O / L[:, None]
         if gate is not None:
-            out[r] *= 1.0 / (1.0 + np.exp(-np.asarray(gate[t], dtype=np.float64)))
+            with np.errstate(over="ignore"):                # exp(+huge) = inf gives the closed gate 0
+                out[r] *= 1.0 / (1.0 + np.exp(-np.asarray(gate[t], dtype=np.float64)))
     return out, out.astype(np.float16), part, bad
 
 

@@ -122,19 +122,25 @@ def qsa_select(scores, pos0, ids, budget=2048, sink=64, local=256, stream=None):
     _abi.check(lib().qsa_select(ctypes.byref(a), _stream(stream)))
 
 
-def qsa_attn(q, kq, vq, ksc, vsc, ids, out, softmax_scale=None, part=None, err=None, stream=None):
+def qsa_attn(q, kq, vq, ksc, vsc, ids, out, softmax_scale=None, part=None, err=None, gate=None, stream=None):
     """Chunked attention of q [T, Hq, D] fp16 over ids [T, W] int32 (-1 =
-    padding, W a multiple of 64) into out [T, Hq, D] fp16.  part, if given,
-    is [T, W/64, Hq, D+2] fp32 and selects the split per-chunk + merge path."""
+    padding, W a multiple of 64) into out [T, Hq, D] fp16.  kq/vq are
+    [cells, D] (one KV head) or [cells, Hkv, D] int8, scales [cells, (Hkv,)
+    4] fp16; D is 128 (32-dim groups) or 256 (64-dim groups).  gate, if
+    given, is [T, Hq, D] fp32 logits: out = fp16(O * sigmoid(gate)).  part,
+    if given, is [T, W/64, Hq, D+2] fp32 and selects the split per-chunk +
+    merge path."""
     import torch
     T, H, D = q.shape
+    hkv = 1 if kq.dim() == 2 else kq.shape[1]
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
-    a = _abi.AttnArgs(ntok=T, n_q_heads=H, n_kv_heads=1, head_dim=D, group=32, cache_cells=kq.shape[0],
+    a = _abi.AttnArgs(ntok=T, n_q_heads=H, n_kv_heads=hkv, head_dim=D, group=D // 4, cache_cells=kq.shape[0],
                       width=ids.shape[1], q=_ptr(q, "q", torch.float16), kq=_ptr(kq, "kq", torch.int8),
                       vq=_ptr(vq, "vq", torch.int8), ksc=_ptr(ksc, "ksc", torch.float16),
                       vsc=_ptr(vsc, "vsc", torch.float16), ids=_ptr(ids, "ids", torch.int32),
                       softmax_scale=float(softmax_scale), out=_ptr(out, "out", torch.float16),
                       part=_ptr(part, "part", torch.float32, optional=True),
-                      err=_ptr(err, "err", torch.int32, optional=True))
+                      err=_ptr(err, "err", torch.int32, optional=True),
+                      gate=_ptr(gate, "gate", torch.float32, optional=True))
     _abi.check(lib().qsa_attn(ctypes.byref(a), _stream(stream)))

@@ -46,7 +46,7 @@ class AttnArgs(ctypes.Structure):
     _fields_ = [("ntok", _c_int), ("n_q_heads", _c_int), ("n_kv_heads", _c_int), ("head_dim", _c_int),
                 ("group", _c_int), ("cache_cells", _c_int), ("width", _c_int),
                 ("q", _vp), ("kq", _vp), ("vq", _vp), ("ksc", _vp), ("vsc", _vp), ("ids", _vp),
-                ("softmax_scale", _c_float), ("out", _vp), ("part", _vp), ("err", _vp)]
+                ("softmax_scale", _c_float), ("out", _vp), ("part", _vp), ("err", _vp), ("gate", _vp)]
 
 
 class QSAError(RuntimeError):
@@ -55,6 +55,7 @@ class QSAError(RuntimeError):
         self.status = status
 
 
+ABI_VERSION = 2  # the struct layouts above
 _lib = None
 
 
@@ -80,6 +81,9 @@ def lib() -> ctypes.CDLL:
         L.qsa_last_error.restype = ctypes.c_char_p
         L.qsa_abi_version.argtypes = []
         L.qsa_abi_version.restype = _c_int
+        if L.qsa_abi_version() != ABI_VERSION:
+            raise RuntimeError(f"{LIB_PATH} has ABI version {L.qsa_abi_version()}, these bindings expect "
+                               f"{ABI_VERSION}: rebuild it")
         _lib = L
     return _lib
 

@@ -125,9 +125,12 @@ qsa_status qsa_attn(const qsa_attn_args *a, void *stream) {
     g_last_error[0] = 0;
     if (!a) return fail(QSA_ERR_INVALID_ARG, "qsa_attn: args is NULL");
     if (a->ntok < 0 || a->cache_cells < 1) return fail(QSA_ERR_INVALID_ARG, "qsa_attn: negative ntok or empty cache");
-    if (a->head_dim != kHeadDim || a->group != kGroup || a->n_kv_heads != 1 || a->n_q_heads < 1 ||
-        a->n_q_heads > 16)
-        return fail(QSA_ERR_UNSUPPORTED, "qsa_attn: supported shapes are head_dim 128, group 32, 1 KV head, 1..16 query heads");
+    const bool shape128 = a->head_dim == 128 && a->group == 32, shape256 = a->head_dim == 256 && a->group == 64;
+    if (!(shape128 || shape256) || a->n_kv_heads < 1 || a->n_q_heads < 1 || a->n_q_heads % a->n_kv_heads != 0 ||
+        a->n_q_heads / a->n_kv_heads > 16 || a->n_kv_heads > 65535)
+        return fail(QSA_ERR_UNSUPPORTED,
+                    "qsa_attn: supported shapes are (head_dim 128, group 32) or (head_dim 256, group 64), "
+                    "n_q_heads a multiple of n_kv_heads with at most 16 query heads per KV head");
     if (a->width <= 0 || a->width % 64 != 0)
         return fail(QSA_ERR_INVALID_ARG, "qsa_attn: width must be a positive multiple of 64");
     if (!std::isfinite(a->softmax_scale)) return fail(QSA_ERR_INVALID_ARG, "qsa_attn: softmax_scale not finite");
@@ -135,10 +138,12 @@ qsa_status qsa_attn(const qsa_attn_args *a, void *stream) {
     if (!a->q || !a->kq || !a->vq || !a->ksc || !a->vsc || !a->ids || !a->out)
         return fail(QSA_ERR_INVALID_ARG, "qsa_attn: NULL buffer");
     if (!aligned(a->q, 16) || !aligned(a->kq, 16) || !aligned(a->vq, 16) || !aligned(a->ksc, 8) ||
-        !aligned(a->vsc, 8) || !aligned(a->ids, 4) || !aligned(a->out, 16) || (a->part && !aligned(a->part, 16)))
+        !aligned(a->vsc, 8) || !aligned(a->ids, 4) || !aligned(a->out, 16) || (a->part && !aligned(a->part, 16)) ||
+        (a->gate && !aligned(a->gate, 4)))
         return fail(QSA_ERR_INVALID_ARG, "qsa_attn: misaligned buffer");
-    qsa::AttnLaunch L{a->ntok, a->n_q_heads, a->cache_cells, a->width, a->q,  a->kq,   a->vq, a->ksc,
-                      a->vsc,  a->ids,       a->softmax_scale, a->out, a->part, a->err};
+    qsa::AttnLaunch L{a->ntok,   a->n_q_heads, a->cache_cells, a->width, a->q,          a->kq,
+                      a->vq,     a->ksc,       a->vsc,         a->ids,   a->softmax_scale, a->out,
+                      a->part,   a->err,       a->n_kv_heads,  a->head_dim, a->gate};
     cudaError_t e = qsa::launch_attn(L, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_attn");
 }

@@ -27,6 +27,16 @@
 // are merged max-first in shared memory.  Split path (part != NULL): one warp
 // per 64-cell chunk writes that chunk's (o_c, m_c, l_c); a second kernel merges
 // the chunks max-first exactly as the definition states.
+//
+// Several KV heads ("round 5 track b ...", section "mtp attention": a grid of
+// two KV heads per token, 12 query heads on each) become a second grid
+// dimension: a CTA serves one (token, KV head).  The pages' head_dim 256 with
+// per-64 scales keeps four scale groups per row; two warps share each unit,
+// each staging, converting and multiplying only its 128-dim half of every K
+// and V row.  Their partial Q.K^T sums meet in shared memory (one 64-thread
+// named barrier per unit), and both warps add them, so they hold identical
+// scores and softmax state; each then accumulates P.V for its half of the
+// dims.  An optional sigmoid output gate multiplies the merged result.
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
@@ -36,8 +46,7 @@
 namespace qsa {
 namespace {
 
-constexpr int D = 128;
-constexpr int G = 32;
+constexpr int D = 128;     // dims one warp handles (the whole row when head_dim is 128)
 constexpr int UNIT = 32;   // cells per warp step
 constexpr int CHUNK = 64;  // cells per chunk of the definition
 constexpr float LN2 = 0.6931471805599453f;
@@ -66,6 +75,66 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+// Where a warp's data lives.  KV head kvh serves query heads h0 .. h0+per-1;
+// with S warps sharing a unit, warp part `half` owns dims [128 half, 128 half
+// + 128) of rows of S * 128 dims.  Scales are four fp16 per (cell, KV head).
+struct Geom {
+    int kvh, h0, per, half;
+};
+
+__device__ __forceinline__ Geom make_geom(const AttnLaunch &a, int half) {
+    Geom g;
+    g.kvh = blockIdx.y;
+    g.per = a.n_q_heads / a.n_kv_heads;
+    g.h0 = g.kvh * g.per;
+    g.half = half;
+    return g;
+}
+
+template <int S>
+__device__ __forceinline__ size_t kv_row(const AttnLaunch &a, const Geom &g, int c) {
+    return ((size_t)c * a.n_kv_heads + g.kvh) * (D * S) + D * g.half;
+}
+__device__ __forceinline__ size_t scale_row(const AttnLaunch &a, const Geom &g, int c) {
+    return ((size_t)c * a.n_kv_heads + g.kvh) * 4;
+}
+// Scale group of quad lane r's 32 K dims and of lane group g's 16 V dims.
+template <int S>
+__device__ __forceinline__ int kgroup(int r, int half) {
+    return S == 1 ? r : 2 * half + (r >> 1);
+}
+template <int S>
+__device__ __forceinline__ int vgroup(int g, int half) {
+    return S == 1 ? (g >> 1) : 2 * half + (g >> 2);
+}
+
+// With S == 2 the two warps of a unit (warps 2p, 2p+1) each hold Q.K^T over
+// their half of the contraction; after this both hold the full sums, equal
+// bit for bit (floating-point addition commutes).  `xch` holds two parity
+// slots of 16 floats x 32 lanes per warp; one named barrier per unit suffices
+// because a slot is rewritten only after the partner passed the next barrier.
+template <int S>
+__device__ __forceinline__ void exchange_s(float (&s)[4][4], float *xch, int parity) {
+    if constexpr (S == 2) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        float *mine = xch + (warp * 2 + parity) * 16 * 32 + lane;
+        const float *other = xch + ((warp ^ 1) * 2 + parity) * 16 * 32 + lane;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mine[(4 * j + e) * 32] = s[j][e];
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp >> 1)) : "memory");
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[j][e] += other[(4 * j + e) * 32];
+    }
+}
+
+__device__ __forceinline__ float gated(const AttnLaunch &a, size_t idx, float v) {
+    return a.gate ? v * (1.0f / (1.0f + expf(-__ldg(a.gate + idx)))) : v;
+}
+
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -92,14 +161,16 @@ __device__ __forceinline__ void state_init(State &st) {
 
 // Q fragments of token t for the permuted contraction: slot 2r+e of k-step ks
 // holds d = 32r + 4ks + e, slot 2r+8+e holds d = 32r + 4ks + 2 + e.
-__device__ __forceinline__ void load_q(const AttnLaunch &a, int t, uint32_t (&qa)[8][4]) {
+template <int S>
+__device__ __forceinline__ void load_q(const AttnLaunch &a, int t, const Geom &geo, uint32_t (&qa)[8][4]) {
     const int lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
         const int h = g + 8 * half;
         uint32_t w[16];
-        if (h < a.n_q_heads) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((size_t)t * a.n_q_heads + h) * D + 32 * r);
+        if (h < geo.per) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                a.q + ((size_t)t * a.n_q_heads + geo.h0 + h) * (D * S) + D * geo.half + 32 * r);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint4 v = __ldg(src + i);
@@ -134,9 +205,9 @@ struct QRegs {
 // One 32-cell unit (id slots slot0 .. slot0+31, lane's id already loaded)
 // folded into the warp's state.  sl2 = softmax_scale * log2(e).  Sets `bad`
 // if an id was < -1 or >= cache_cells.
-template <class Q>
+template <int S, class Q>
 __device__ __forceinline__ void process_unit(const AttnLaunch &a, int id, const Q &qsrc, State &st, float sl2,
-                                             bool &bad) {
+                                             bool &bad, const Geom &geo, float *xch, int parity) {
     const int lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
     const bool valid = id >= 0 && id < a.cache_cells;
     bad |= (id < -1) || (id >= a.cache_cells);
@@ -152,10 +223,10 @@ __device__ __forceinline__ void process_unit(const AttnLaunch &a, int id, const 
     for (int j = 0; j < 4; ++j) {
         const int c = __shfl_sync(0xffffffffu, id, 8 * j + g);
         if (c >= 0) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.kq + (size_t)c * D + 32 * r);
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.kq + kv_row<S>(a, geo, c) + 32 * r);
             kd[j][0] = __ldg(src);
             kd[j][1] = __ldg(src + 1);
-            ks[j] = __ushort_as_half(__ldg(a.ksc + (size_t)c * (D / G) + r));
+            ks[j] = __ushort_as_half(__ldg(a.ksc + scale_row(a, geo, c) + kgroup<S>(r, geo.half)));
         } else {
             kd[j][0] = kd[j][1] = make_uint4(0u, 0u, 0u, 0u);
             ks[j] = __ushort_as_half(0);
@@ -169,8 +240,8 @@ __device__ __forceinline__ void process_unit(const AttnLaunch &a, int id, const 
         for (int e = 0; e < 4; ++e) {
             const int c = __shfl_sync(0xffffffffu, id, 16 * kk + 2 * r + (e & 1) + 8 * (e >> 1));
             if (c >= 0) {
-                vd[kk][e] = __ldg(reinterpret_cast<const uint4 *>(a.vq + (size_t)c * D + 16 * g));
-                vs[kk][e] = __ushort_as_half(__ldg(a.vsc + (size_t)c * (D / G) + (g >> 1)));
+                vd[kk][e] = __ldg(reinterpret_cast<const uint4 *>(a.vq + kv_row<S>(a, geo, c) + 16 * g));
+                vs[kk][e] = __ushort_as_half(__ldg(a.vsc + scale_row(a, geo, c) + vgroup<S>(g, geo.half)));
             } else {
                 vd[kk][e] = make_uint4(0u, 0u, 0u, 0u);
                 vs[kk][e] = __ushort_as_half(0);
@@ -195,6 +266,7 @@ __device__ __forceinline__ void process_unit(const AttnLaunch &a, int id, const 
             mma16816(s[j], qf, h2u(__hmul2(lo, sc)), h2u(__hmul2(hi, sc)));
         }
     }
+    exchange_s<S>(s, xch, parity);
 
     // Online softmax in base 2 over this unit's valid cells.
     float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
@@ -302,27 +374,28 @@ __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0
 
 // Issue the copies of one unit into stage `st` (shared address).  `id` is the
 // lane's id slot (already mapped to -1 when invalid).
-__device__ __forceinline__ void issue_unit(const AttnLaunch &a, int id, uint32_t st) {
+template <int S>
+__device__ __forceinline__ void issue_unit(const AttnLaunch &a, int id, uint32_t st, const Geom &geo) {
     const int lane = threadIdx.x & 31, q = lane & 7;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int cell = (lane >> 3) + 4 * i;
         const int c = __shfl_sync(0xffffffffu, id, cell);
         const bool ok = c >= 0;
-        const size_t off = (size_t)(ok ? c : 0) * D + 16 * q;
+        const size_t off = kv_row<S>(a, geo, ok ? c : 0) + 16 * q;
         cp_async16(st + cell * D + ((q ^ (cell & 1)) << 4), a.kq + off, ok);
         cp_async16(st + UNIT * D + cell * D + ((q ^ (2 * ((cell >> 1) & 3))) << 4), a.vq + off, ok);
     }
     const bool ok = id >= 0;
-    const size_t so = (size_t)(ok ? id : 0) * (D / G);
+    const size_t so = scale_row(a, geo, ok ? id : 0);
     cp_async8(st + 2 * UNIT * D + lane * 8, a.ksc + so, ok);
     cp_async8(st + 2 * UNIT * D + UNIT * 8 + lane * 8, a.vsc + so, ok);
 }
 
 // Compute one staged unit.  vmask: valid cells of the unit.
-template <class Q>
+template <int S, class Q>
 __device__ __forceinline__ void compute_staged(const uint8_t *stp, unsigned vmask, const Q &qsrc, State &st,
-                                               float sl2) {
+                                               float sl2, int dhalf, float *xch, int parity) {
     const int lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
     const uint8_t *K = stp, *V = stp + UNIT * D;
     const __half *KS = reinterpret_cast<const __half *>(stp + 2 * UNIT * D);
@@ -339,7 +412,7 @@ __device__ __forceinline__ void compute_staged(const uint8_t *stp, unsigned vmas
         for (int j = 0; j < 4; ++j) {
             const int cell = 8 * j + g;
             kd[j] = *reinterpret_cast<const uint4 *>(K + cell * D + (((2 * r + half) ^ (cell & 1)) << 4));
-            sc[j] = __half2half2(KS[cell * 4 + r]);
+            sc[j] = __half2half2(KS[cell * 4 + kgroup<S>(r, dhalf)]);
         }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -353,6 +426,7 @@ __device__ __forceinline__ void compute_staged(const uint8_t *stp, unsigned vmas
             }
         }
     }
+    exchange_s<S>(s, xch, parity);
 
     float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
 #pragma unroll
@@ -409,7 +483,7 @@ __device__ __forceinline__ void compute_staged(const uint8_t *stp, unsigned vmas
         for (int e = 0; e < 4; ++e) {
             const int cell = 16 * kk + 2 * r + (e & 1) + 8 * (e >> 1);
             vd[e] = *reinterpret_cast<const uint4 *>(V + cell * D + ((g ^ (2 * ((cell >> 1) & 3))) << 4));
-            vs[e] = VS[cell * 4 + (g >> 1)];
+            vs[e] = VS[cell * 4 + vgroup<S>(g, dhalf)];
         }
         const __half2 v01 = __halves2half2(vs[0], vs[1]);
         const __half2 v89 = __halves2half2(vs[2], vs[3]);
@@ -434,36 +508,47 @@ __device__ __forceinline__ void compute_staged(const uint8_t *stp, unsigned vmas
 #define QSA_ATTN_NS 2
 #endif
 
-template <int NW, int NS>
+// Exchange slots for S == 2: per warp, two parities of 16 floats x 32 lanes.
+template <int NW, int S>
+constexpr int xch_bytes() {
+    return S == 2 ? NW * 2 * 16 * 32 * (int)sizeof(float) : 0;
+}
+
+template <int NW, int NS, int S>
 __global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(AttnLaunch a) {
     extern __shared__ __align__(16) uint8_t smem8[];
+    constexpr int NP = NW / S;  // unit groups per CTA
     const int t = a.ntok - 1 - (int)blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
+    const int pw = warp / S, half = warp % S;
+    const Geom geo = make_geom(a, half);
     const float sl2 = a.softmax_scale * LOG2E;
     const int32_t *idrow = a.ids + (size_t)t * a.width;
     const int nunits = a.width / UNIT;
     uint8_t *ring = smem8 + warp * NS * STAGE_BYTES;
     const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+    float *xch = reinterpret_cast<float *>(smem8 + NW * NS * STAGE_BYTES);
     QRegs qsrc;
-    load_q(a, t, qsrc.qa);
+    load_q<S>(a, t, geo, qsrc.qa);
     State st;
     state_init(st);
     bool bad = false;
 
-    // My units are u_i = warp + i*NW, i = 0 .. n-1.
-    const int n = warp < nunits ? (nunits - warp + NW - 1) / NW : 0;
+    // My group's units are u_i = pw + i*NP, i = 0 .. n-1.
+    const int n = pw < nunits ? (nunits - pw + NP - 1) / NP : 0;
     auto unit_id = [&](int i) -> int {
         if (i >= n) return -1;
-        int id = __ldg(idrow + (warp + i * NW) * UNIT + lane);
+        int id = __ldg(idrow + (pw + i * NP) * UNIT + lane);
         bad |= (id < -1) || (id >= a.cache_cells);
         return (id >= 0 && id < a.cache_cells) ? id : -1;
     };
+    int nx = 0;   // exchanges so far: their parity picks the slot (skipped units exchange nothing)
     int idq[NS];  // ids of units i .. i+NS-1 (ring of registers)
 #pragma unroll
     for (int k = 0; k < NS; ++k) idq[k] = unit_id(k);
 #pragma unroll
     for (int k = 0; k < NS - 1; ++k) {
-        if (__any_sync(0xffffffffu, idq[k] >= 0)) issue_unit(a, idq[k], ring_s + k * STAGE_BYTES);
+        if (__any_sync(0xffffffffu, idq[k] >= 0)) issue_unit<S>(a, idq[k], ring_s + k * STAGE_BYTES, geo);
         cp_commit();
     }
     for (int i = 0; i < n; ++i) {
@@ -476,12 +561,13 @@ __global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(Att
             if (k == sI) id_i = idq[k];
             if (k == sN) id_n = idq[k];
         }
-        if (__any_sync(0xffffffffu, id_n >= 0) && i + NS - 1 < n) issue_unit(a, id_n, ring_s + sN * STAGE_BYTES);
+        if (__any_sync(0xffffffffu, id_n >= 0) && i + NS - 1 < n)
+            issue_unit<S>(a, id_n, ring_s + sN * STAGE_BYTES, geo);
         cp_commit();
         cp_wait<NS - 1>();
         __syncwarp();
-        const unsigned vmask = __ballot_sync(0xffffffffu, id_i >= 0);
-        if (vmask) compute_staged(ring + sI * STAGE_BYTES, vmask, qsrc, st, sl2);
+        const unsigned vmask = __ballot_sync(0xffffffffu, id_i >= 0);  // the same in both warps of a group
+        if (vmask) compute_staged<S>(ring + sI * STAGE_BYTES, vmask, qsrc, st, sl2, half, xch, nx++ & 1);
         __syncwarp();
         const int nid = unit_id(i + NS);
 #pragma unroll
@@ -493,120 +579,143 @@ __global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(Att
     quad_sum_l(st);
     __syncthreads();
 
-    // Merge: reuse the rings (all copies have landed) for the per-warp states.
+    // Merge: reuse the rings (all copies have landed) for the groups' states.
+    constexpr int DR = D * S;  // row length
     float *so = reinterpret_cast<float *>(smem8);
-    float *sm = so + NW * 16 * D;
-    float *sl = sm + NW * 16;
-    float *ow = so + warp * 16 * D;
+    float *sm = so + NP * 16 * DR;
+    float *sl = sm + NP * 16;
+    float *ow = so + pw * 16 * DR + D * half;
 #pragma unroll
     for (int jd = 0; jd < 16; ++jd) {
-        ow[g * D + 32 * r + jd] = st.o[jd][0];
-        ow[g * D + 32 * r + 16 + jd] = st.o[jd][1];
-        ow[(g + 8) * D + 32 * r + jd] = st.o[jd][2];
-        ow[(g + 8) * D + 32 * r + 16 + jd] = st.o[jd][3];
+        ow[g * DR + 32 * r + jd] = st.o[jd][0];
+        ow[g * DR + 32 * r + 16 + jd] = st.o[jd][1];
+        ow[(g + 8) * DR + 32 * r + jd] = st.o[jd][2];
+        ow[(g + 8) * DR + 32 * r + 16 + jd] = st.o[jd][3];
     }
-    if (r == 0) {
-        sm[warp * 16 + g] = st.m[0];
-        sm[warp * 16 + g + 8] = st.m[1];
-        sl[warp * 16 + g] = st.l[0];
-        sl[warp * 16 + g + 8] = st.l[1];
+    if (r == 0 && half == 0) {
+        sm[pw * 16 + g] = st.m[0];
+        sm[pw * 16 + g + 8] = st.m[1];
+        sl[pw * 16 + g] = st.l[0];
+        sl[pw * 16 + g + 8] = st.l[1];
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < a.n_q_heads * D; idx += NW * 32) {
-        const int h = idx / D, d = idx % D;
+    for (int idx = threadIdx.x; idx < geo.per * DR; idx += NW * 32) {
+        const int h = idx / DR, d = idx % DR;
         float M = -CUDART_INF_F;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm[w * 16 + h]);
+        for (int w = 0; w < NP; ++w) M = fmaxf(M, sm[w * 16 + h]);
         float res = 0.0f;
         if (M != -CUDART_INF_F) {
             float L = 0.0f, O = 0.0f;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
+            for (int w = 0; w < NP; ++w) {
                 const float mw = sm[w * 16 + h];
                 if (mw == -CUDART_INF_F) continue;
                 const float sc = exp2f(mw - M);
                 L += sc * sl[w * 16 + h];
-                O += sc * so[(w * 16 + h) * D + d];
+                O += sc * so[(w * 16 + h) * DR + d];
             }
             res = O / L;
         }
-        a.out[((size_t)t * a.n_q_heads + h) * D + d] = __half_as_ushort(__float2half_rn(res));
+        const size_t oi = ((size_t)t * a.n_q_heads + geo.h0 + h) * DR + d;
+        a.out[oi] = __half_as_ushort(__float2half_rn(gated(a, oi, res)));
     }
 }
 
-// Split path, part 1: one warp per (token, 64-cell chunk) writes the chunk's
-// unnormalised values, maximum (natural-log units) and denominator.
-template <int NW>
+// Split path, part 1: one group of S warps per (token, KV head, 64-cell
+// chunk) writes the chunk's unnormalised values, maximum (natural-log units)
+// and denominator.
+template <int NW, int S>
 __global__ void __launch_bounds__(NW * 32) attn_chunk_kernel(AttnLaunch a) {
+    constexpr int NP = NW / S;
+    constexpr int DR = D * S;
+    __shared__ float xch[S == 2 ? NW * 2 * 16 * 32 : 1];
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
+    const int pw = warp / S, half = warp % S;
+    const Geom geo = make_geom(a, half);
     const int nch = a.width / CHUNK;
-    const int c = blockIdx.y * NW + warp;
-    if (c >= nch) return;
+    const int c = blockIdx.z * NP + pw;
+    if (c >= nch) return;  // both warps of a group leave together
     const float sl2 = a.softmax_scale * LOG2E;
     const int32_t *idrow = a.ids + (size_t)t * a.width;
     QRegs qsrc;
-    load_q(a, t, qsrc.qa);
+    load_q<S>(a, t, geo, qsrc.qa);
     State st;
     state_init(st);
     bool bad = false;
     const int id0 = __ldg(idrow + c * CHUNK + lane), id1 = __ldg(idrow + c * CHUNK + UNIT + lane);
-    process_unit(a, id0, qsrc, st, sl2, bad);
-    process_unit(a, id1, qsrc, st, sl2, bad);
+    process_unit<S>(a, id0, qsrc, st, sl2, bad, geo, xch, 0);
+    process_unit<S>(a, id1, qsrc, st, sl2, bad, geo, xch, 1);
     if (__any_sync(0xffffffffu, bad) && lane == 0 && a.err) atomicOr(a.err, QSA_DEVERR_BAD_ID);
     quad_sum_l(st);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int h = g + 8 * half;
-        if (h >= a.n_q_heads) continue;
-        float *dst = a.part + (((size_t)t * nch + c) * a.n_q_heads + h) * (D + 2);
+    for (int hf = 0; hf < 2; ++hf) {
+        const int h = g + 8 * hf;
+        if (h >= geo.per) continue;
+        float *dst = a.part + (((size_t)t * nch + c) * a.n_q_heads + geo.h0 + h) * (DR + 2);
 #pragma unroll
         for (int jd = 0; jd < 16; ++jd) {
-            dst[32 * r + jd] = st.o[jd][2 * half];
-            dst[32 * r + 16 + jd] = st.o[jd][2 * half + 1];
+            dst[D * half + 32 * r + jd] = st.o[jd][2 * hf];
+            dst[D * half + 32 * r + 16 + jd] = st.o[jd][2 * hf + 1];
         }
-        if (r == 0) {
-            const float mm = st.m[half];
-            dst[D] = mm == -CUDART_INF_F ? mm : mm * LN2;
-            dst[D + 1] = st.l[half];
+        if (r == 0 && half == 0) {
+            const float mm = st.m[hf];
+            dst[DR] = mm == -CUDART_INF_F ? mm : mm * LN2;
+            dst[DR + 1] = st.l[hf];
         }
     }
 }
 
 // Split path, part 2: max-first merge of the chunk partials of one token.
-__global__ void __launch_bounds__(D) attn_merge_kernel(AttnLaunch a) {
+template <int S>
+__global__ void __launch_bounds__(D * S) attn_merge_kernel(AttnLaunch a) {
+    constexpr int DR = D * S;
     const int t = blockIdx.x, d = threadIdx.x;
     const int nch = a.width / CHUNK;
     for (int h = 0; h < a.n_q_heads; ++h) {
-        const float *base = a.part + ((size_t)t * nch * a.n_q_heads + h) * (D + 2);
-        const size_t cstride = (size_t)a.n_q_heads * (D + 2);
+        const float *base = a.part + ((size_t)t * nch * a.n_q_heads + h) * (DR + 2);
+        const size_t cstride = (size_t)a.n_q_heads * (DR + 2);
         float M = -CUDART_INF_F;
-        for (int c = 0; c < nch; ++c) M = fmaxf(M, base[c * cstride + D]);
+        for (int c = 0; c < nch; ++c) M = fmaxf(M, base[c * cstride + DR]);
         float res = 0.0f;
         if (M != -CUDART_INF_F) {
             float L = 0.0f, O = 0.0f;
             for (int c = 0; c < nch; ++c) {
-                const float mc = base[c * cstride + D];
+                const float mc = base[c * cstride + DR];
                 if (mc == -CUDART_INF_F) continue;
                 const float w = expf(mc - M);
-                L += w * base[c * cstride + D + 1];
+                L += w * base[c * cstride + DR + 1];
                 O += w * base[c * cstride + d];
             }
             res = O / L;
         }
-        a.out[((size_t)t * a.n_q_heads + h) * D + d] = __half_as_ushort(__float2half_rn(res));
+        const size_t oi = ((size_t)t * a.n_q_heads + h) * DR + d;
+        a.out[oi] = __half_as_ushort(__float2half_rn(gated(a, oi, res)));
     }
 }
 
-template <int NW, int NS>
+template <int NW, int NS, int S>
 cudaError_t launch_staged(const AttnLaunch &a, cudaStream_t s) {
-    size_t smem = (size_t)NW * NS * STAGE_BYTES;
-    const size_t merge = (size_t)NW * (16 * D + 32) * sizeof(float);
+    size_t smem = (size_t)NW * NS * STAGE_BYTES + xch_bytes<NW, S>();
+    const size_t merge = (size_t)(NW / S) * (16 * D * S + 32) * sizeof(float);
     if (smem < merge) smem = merge;
-    cudaError_t e = cudaFuncSetAttribute(attn_staged_kernel<NW, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(attn_staged_kernel<NW, NS, S>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attn_staged_kernel<NW, NS><<<a.ntok, NW * 32, smem, s>>>(a);
+    attn_staged_kernel<NW, NS, S><<<dim3(a.ntok, a.n_kv_heads), NW * 32, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int S>
+cudaError_t launch_split(const AttnLaunch &a, cudaStream_t s) {
+    constexpr int NW = 4;
+    const int nch = a.width / CHUNK;
+    dim3 grid(a.ntok, a.n_kv_heads, (nch + NW / S - 1) / (NW / S));
+    attn_chunk_kernel<NW, S><<<grid, NW * 32, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    attn_merge_kernel<S><<<a.ntok, D * S, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -614,26 +723,18 @@ cudaError_t launch_staged(const AttnLaunch &a, cudaStream_t s) {
 
 cudaError_t launch_attn(const AttnLaunch &a, cudaStream_t s) {
     if (a.ntok == 0) return cudaSuccess;
-    if (a.part) {
-        constexpr int NW = 4;
-        const int nch = a.width / CHUNK;
-        dim3 grid(a.ntok, (nch + NW - 1) / NW);
-        attn_chunk_kernel<NW><<<grid, NW * 32, 0, s>>>(a);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        attn_merge_kernel<<<a.ntok, D, 0, s>>>(a);
-        return cudaGetLastError();
-    }
+    const bool wide = a.head_dim == 2 * D;
+    if (a.part) return wide ? launch_split<2>(a, s) : launch_split<1>(a, s);
 #ifndef QSA_ATTN_TC
 #define QSA_ATTN_TC 0
 #endif
 #if QSA_ATTN_TC
-    return launch_attn_tc(a, s);
+    if (!wide && a.n_kv_heads == 1 && !a.gate) return launch_attn_tc(a, s);
 #endif
 #ifndef QSA_ATTN_NW
 #define QSA_ATTN_NW 4
 #endif
-    return launch_staged<QSA_ATTN_NW, QSA_ATTN_NS>(a, s);
+    return wide ? launch_staged<QSA_ATTN_NW, QSA_ATTN_NS, 2>(a, s) : launch_staged<QSA_ATTN_NW, QSA_ATTN_NS, 1>(a, s);
 }
 
 }  // namespace qsa

@@ -41,6 +41,8 @@ struct AttnLaunch {
     uint16_t *out;
     float *part;
     unsigned int *err;
+    int n_kv_heads, head_dim;  // head_dim 128 (group 32) or 256 (group 64): four scale groups per row
+    const float *gate;         // NULL or [ntok, n_q_heads, head_dim] output-gate logits
 };
 
 struct SelectLaunch {
