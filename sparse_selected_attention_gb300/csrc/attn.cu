@@ -80,23 +80,30 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
 // + 128) of rows of S * 128 dims.  Scales are four fp16 per (cell, KV head).
 struct Geom {
     int kvh, h0, per, half;
+    int kstride, koff;  // code row of cell c starts at c * kstride + koff
+    int sstride, soff;  // its four scales at c * sstride + soff
 };
 
+template <int S>
 __device__ __forceinline__ Geom make_geom(const AttnLaunch &a, int half) {
     Geom g;
     g.kvh = blockIdx.y;
     g.per = a.n_q_heads / a.n_kv_heads;
     g.h0 = g.kvh * g.per;
     g.half = half;
+    g.kstride = a.n_kv_heads * D * S;
+    g.koff = g.kvh * D * S + D * half;
+    g.sstride = a.n_kv_heads * 4;
+    g.soff = g.kvh * 4;
     return g;
 }
 
 template <int S>
-__device__ __forceinline__ size_t kv_row(const AttnLaunch &a, const Geom &g, int c) {
-    return ((size_t)c * a.n_kv_heads + g.kvh) * (D * S) + D * g.half;
+__device__ __forceinline__ size_t kv_row(const AttnLaunch &, const Geom &g, int c) {
+    return (size_t)c * g.kstride + g.koff;
 }
-__device__ __forceinline__ size_t scale_row(const AttnLaunch &a, const Geom &g, int c) {
-    return ((size_t)c * a.n_kv_heads + g.kvh) * 4;
+__device__ __forceinline__ size_t scale_row(const AttnLaunch &, const Geom &g, int c) {
+    return (size_t)c * g.sstride + g.soff;
 }
 // Scale group of quad lane r's 32 K dims and of lane group g's 16 V dims.
 template <int S>
@@ -521,7 +528,7 @@ __global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(Att
     const int t = a.ntok - 1 - (int)blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
     const int pw = warp / S, half = warp % S;
-    const Geom geo = make_geom(a, half);
+    const Geom geo = make_geom<S>(a, half);
     const float sl2 = a.softmax_scale * LOG2E;
     const int32_t *idrow = a.ids + (size_t)t * a.width;
     const int nunits = a.width / UNIT;
@@ -633,7 +640,7 @@ __global__ void __launch_bounds__(NW * 32) attn_chunk_kernel(AttnLaunch a) {
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
     const int pw = warp / S, half = warp % S;
-    const Geom geo = make_geom(a, half);
+    const Geom geo = make_geom<S>(a, half);
     const int nch = a.width / CHUNK;
     const int c = blockIdx.z * NP + pw;
     if (c >= nch) return;  // both warps of a group leave together
