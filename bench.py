@@ -290,11 +290,13 @@ def run_ours(args, rank, world, local_rank):
     names = KERNELS_SELECT if args.select else KERNELS
     nk = len(names)
 
-    def step(ev=None):
+    main_bufs = {"q": q_in, "k": k_in, "v": v_in, "ids": ids, "out": out}
+
+    def step(ev=None, b=main_bufs):
         i = 0
         if ev:
             ev[i].record(stream)
-        qsa_prep(q_in, k_in, v_in, norm_w, pos0, kq, vq, ksc, vsc, q16, q_out_f32=q32)
+        qsa_prep(b["q"], b["k"], b["v"], norm_w, pos0, kq, vq, ksc, vsc, q16, q_out_f32=q32)
         i += 1
         if ev:
             ev[i].record(stream)
@@ -303,11 +305,11 @@ def run_ours(args, rank, world, local_rank):
             i += 1
             if ev:
                 ev[i].record(stream)
-            qsa_select(scores, pos0, ids)
+            qsa_select(scores, pos0, b["ids"])
         i += 1
         if ev:
             ev[i].record(stream)
-        qsa_attn(q16, kq, vq, ksc, vsc, ids, out)
+        qsa_attn(q16, kq, vq, ksc, vsc, b["ids"], b["out"])
         if ev:
             ev[i + 1].record(stream)
 
@@ -338,41 +340,67 @@ def run_ours(args, rank, world, local_rank):
     step_ms = [evs[k][0].elapsed_time(evs[k][nk]) for k in range(K)]
     ms = max_over_ranks(sum(step_ms) / K, dev)
 
-    # End to end through the public API: H2D of the step's inputs from pinned
-    # host memory, the three calls, D2H of the attention output.
+    # End to end through the public API, as a serving loop runs it: every
+    # step uploads its inputs from pinned host memory, runs the calls and
+    # reads its attention output back.  Inputs and outputs are double-buffered
+    # so that step k+1's upload and step k's read-back (two copy streams)
+    # overlap step k's kernels; the kernels themselves stay on one stream, so
+    # the shared K/V cache and scratch buffers are never used concurrently.
+    # The timed region spans the first upload to the last read-back.  No L2
+    # flush here: every step writes 246 MB of scores, more than L2 holds.
     e2e = None
     if not args.no_e2e:
         h_q, h_k, h_v = (torch.from_numpy(x).pin_memory() for x in (inp.q_in, inp.k_in, inp.v_in))
         h_ids = torch.from_numpy(ids_np).pin_memory()
-        h_out = torch.empty((T, HQ, D), dtype=torch.float16).pin_memory()
+        h_outs = [torch.empty((T, HQ, D), dtype=torch.float16).pin_memory() for _ in range(2)]
         h_in = (h_q, h_k, h_v) if args.select else (h_q, h_k, h_v, h_ids)  # selected ids are made on the device
         h2d = sum(x.numel() * x.element_size() for x in h_in)
-        d2h = h_out.numel() * h_out.element_size()
+        d2h = h_outs[0].numel() * h_outs[0].element_size()
+        bufs = [main_bufs, {"q": torch.empty_like(q_in), "k": torch.empty_like(k_in), "v": torch.empty_like(v_in),
+                            "ids": ids if args.select else torch.empty_like(ids), "out": torch.empty_like(out)}]
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_up, ev_done, ev_down = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+
+        def pipeline(nsteps, start=None):
+            if start is not None:
+                up.wait_event(start)
+            for k in range(nsteps + 1):
+                if k < nsteps:  # upload step k once step k-2 (same buffers) has finished with them
+                    b = bufs[k % 2]
+                    with torch.cuda.stream(up):
+                        if k >= 2:
+                            up.wait_event(ev_done[k % 2])
+                        b["q"].copy_(h_q, non_blocking=True)
+                        b["k"].copy_(h_k, non_blocking=True)
+                        b["v"].copy_(h_v, non_blocking=True)
+                        if not args.select:
+                            b["ids"].copy_(h_ids, non_blocking=True)
+                        ev_up[k % 2].record(up)
+                if k >= 1:  # step k-1 on the kernel stream, then its read-back
+                    j = k - 1
+                    b = bufs[j % 2]
+                    stream.wait_event(ev_up[j % 2])
+                    if j >= 2:
+                        stream.wait_event(ev_down[j % 2])
+                    step(b=b)
+                    ev_done[j % 2].record(stream)
+                    with torch.cuda.stream(down):
+                        down.wait_event(ev_done[j % 2])
+                        h_outs[j % 2].copy_(b["out"], non_blocking=True)
+                        ev_down[j % 2].record(down)
+            stream.wait_event(ev_down[(nsteps - 1) % 2])
+
+        pipeline(3)
+        torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-
-        def e2e_step():
-            q_in.copy_(h_q, non_blocking=True)
-            k_in.copy_(h_k, non_blocking=True)
-            v_in.copy_(h_v, non_blocking=True)
-            if not args.select:
-                ids.copy_(h_ids, non_blocking=True)
-            step()
-            h_out.copy_(out, non_blocking=True)
-
-        for _ in range(3):
-            flush.zero_()
-            e2e_step()
-        tot = 0.0
-        for _ in range(K):
-            flush.zero_()
-            e0.record(stream)
-            e2e_step()
-            e1.record(stream)
-            e1.synchronize()
-            tot += e0.elapsed_time(e1)
-        e2e_ms = max_over_ranks(tot / K, dev)
+        e0.record(stream)
+        pipeline(K, start=e0)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, dev)
         e2e = {"value": weak_scaling_value(T, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "schedule": "double-buffered: step k+1 upload and step k read-back overlap step k's kernels"}
 
     # Roofline of the dominant kernel.
     avg = {n: sum(v) / K for n, v in per.items()}
