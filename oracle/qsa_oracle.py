@@ -136,13 +136,44 @@ def quantize_rows(x: np.ndarray, group: int = 32):
     return codes.reshape(shp), s16.reshape(shp[:-1] + (D // group,))
 
 
+def rotate_keys_f32(k_in: np.ndarray, pos0: int, rope_theta: float = 10000.0, rope_dims: int = 64):
+    """Optional RoPE on the new key rows before they are quantised.
+
+    Reading (the pages rotate the query rows in norm_rope and say nothing of
+    the keys; rotating keys with the same pairs and angles is the usual RoPE
+    and is offered as an option): for i < h = rope_dims/2 and a = (pos0 + t)
+    * inv_freq_i (exact in float64),
+        c = fp32(cos a), s = fp32(sin a)            (from float64 cos / sin)
+        k'_i     = fp32(fp32(k_i * c) - fp32(k_{i+h} * s))
+        k'_{i+h} = fp32(fp32(k_{i+h} * c) + fp32(k_i * s))
+    every step rounded to float32 in that order.  The rotated values decide
+    the int8 codes, so the arithmetic that makes them is part of the
+    definition: the GPU takes the same float32 steps.  No norm on keys.
+    """
+    k = np.array(k_in, dtype=np.float32, copy=True)
+    T = k.shape[0]
+    half = rope_dims // 2
+    if half == 0:
+        return k
+    pos = (pos0 + np.arange(T, dtype=np.float64))[:, None, None]
+    a = pos * rope_inv_freq(rope_dims, rope_theta).astype(np.float64)[None, None, :]
+    c, sn = np.cos(a).astype(np.float32), np.sin(a).astype(np.float32)
+    lo, hi = k[..., :half].copy(), k[..., half:rope_dims].copy()
+    k[..., :half] = (lo * c).astype(np.float32) - (hi * sn).astype(np.float32)
+    k[..., half:rope_dims] = (hi * c).astype(np.float32) + (lo * sn).astype(np.float32)
+    return k
+
+
 def prep(q_in, k_in, v_in, norm_w, pos0, kq, vq, ksc, vsc, eps=1e-6,
-         rope_theta=10000.0, rope_dims=64, group=32):
+         rope_theta=10000.0, rope_dims=64, group=32, rope_k=False):
     """The whole prep step: queries normalised and rotated, K/V rows
-    quantised into cache rows pos0 .. pos0+T-1 (one KV head).  The cache
-    arrays are updated in place; returns prep_queries' triple."""
+    quantised into cache rows pos0 .. pos0+T-1 (one KV head); with rope_k
+    the key rows are rotated first (rotate_keys_f32).  The cache arrays are
+    updated in place; returns prep_queries' triple."""
     T = q_in.shape[0]
     q64, q16, q32 = prep_queries(q_in, norm_w, pos0, eps, rope_theta, rope_dims)
+    if rope_k:
+        k_in = rotate_keys_f32(k_in, pos0, rope_theta, rope_dims)
     kc, ks = quantize_rows(k_in.reshape(T, -1), group)
     vc, vs = quantize_rows(v_in.reshape(T, -1), group)
     kq[pos0:pos0 + T] = kc

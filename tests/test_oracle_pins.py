@@ -423,3 +423,61 @@ def test_attention_kv_head_slices_are_independent():
     b, _, _, _ = attention(q, cache.kq, vq2, cache.ksc, cache.vsc, ids, 0.0625, group=grp)
     assert np.array_equal(a[:, :12], b[:, :12])
     np.testing.assert_allclose(b[:, 12:], -a[:, 12:], rtol=1e-12, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------
+# prep: optional key rotation
+# ----------------------------------------------------------------------------
+
+from oracle import prep as _prep, rotate_keys_f32  # noqa: E402
+
+
+def _prep_cache(T, pos0, seed, rope_k):
+    inp = wl.prep_inputs(T, seed=seed)
+    c = wl.make_cache(pos0 + T, seed=seed)
+    _prep(inp.q_in, inp.k_in, inp.v_in, inp.norm_w, pos0, c.kq, c.vq, c.ksc, c.vsc, rope_k=rope_k)
+    return inp, c
+
+
+def test_rope_k_at_position_zero_is_the_plain_quantiser():
+    inp, a = _prep_cache(1, 0, 61, rope_k=True)
+    _, b = _prep_cache(1, 0, 61, rope_k=False)
+    assert np.array_equal(a.kq, b.kq) and np.array_equal(a.ksc.view(np.uint16), b.ksc.view(np.uint16))
+    assert np.array_equal(a.vq, b.vq)
+
+
+def test_rope_k_one_hot_row():
+    # k = A e_i (i < 32) at position p rotates to A cos(p f_i) at dim i and
+    # A sin(p f_i) at dim i + 32; each is alone in its 32-dim group, so both
+    # quantise to +-127 with scale fp16(|A cos| / 127), fp16(|A sin| / 127).
+    p, i, A = 977, 5, 3.0
+    k = np.zeros((1, 1, 128), np.float32)
+    k[0, 0, i] = A
+    r = rotate_keys_f32(k, p)
+    ang = p * float(np.float32(10000.0 ** (-2 * i / 64)))
+    assert r[0, 0, i] == np.float32(A) * np.float32(np.cos(ang))
+    assert r[0, 0, i + 32] == np.float32(A) * np.float32(np.sin(ang))
+    assert np.count_nonzero(r) == 2
+    codes, scales = wl_quant(r)
+    assert codes[0, 0, i] == 127 * np.sign(np.cos(ang)) and codes[0, 0, i + 32] == 127 * np.sign(np.sin(ang))
+    assert scales[0, 0, 0] == np.float16(np.float32(abs(A * np.cos(ang))) / np.float32(127))
+    assert np.count_nonzero(codes) == 2
+
+
+def wl_quant(x):
+    from oracle import quantize_rows
+    return quantize_rows(x)
+
+
+def test_rope_k_rotation_preserves_pair_norms_and_composes():
+    k = wl.prep_inputs(4, seed=62).k_in
+    r = rotate_keys_f32(k, 1234).astype(np.float64)
+    k64 = k.astype(np.float64)
+    n0 = k64[..., :32] ** 2 + k64[..., 32:64] ** 2
+    n1 = r[..., :32] ** 2 + r[..., 32:64] ** 2
+    np.testing.assert_allclose(n1, n0, rtol=2e-6)
+    assert np.array_equal(r[..., 64:], k64[..., 64:])
+    # rotating by p1 then p2 is rotating by p1 + p2 (one token: its position is pos0)
+    k1 = k[:1]
+    two = rotate_keys_f32(rotate_keys_f32(k1, 300), 700).astype(np.float64)
+    np.testing.assert_allclose(two, rotate_keys_f32(k1, 1000).astype(np.float64), atol=2e-5)
