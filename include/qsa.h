@@ -67,6 +67,11 @@ typedef enum { QSA_F32 = 0, QSA_F16 = 1 } qsa_dtype;
  * K and V rows t are quantised into cache row pos0 + t, per group of `group`
  * dims: s = fp16_rne(fp32(amax/127)); code = s == 0 ? 0 :
  * clamp(rint_half_even(fp32(x / s)), -127, 127).  Bit-exact by definition.
+ * With rope_k = 1 the key row is first rotated with the same pairs and
+ * angles (no norm), in float32 steps: c = fp32(cos a), s = fp32(sin a) from
+ * double-precision cos / sin, k'[i] = fp32(fp32(k[i] c) - fp32(k[i+h] s)),
+ * k'[i+h] = fp32(fp32(k[i+h] c) + fp32(k[i] s)); the pages rotate only the
+ * query rows, so this is an option (off = 0).
  *
  * Layouts (row-major, contiguous): q_in [ntok, n_q_heads, head_dim] fp32;
  * k_in, v_in [ntok, n_kv_heads, head_dim] fp32; norm_w [head_dim] fp32;
@@ -84,6 +89,7 @@ typedef struct {
     float *q_out_f32;
     int8_t *kq, *vq;
     uint16_t *ksc, *vsc;
+    int rope_k; /* added in ABI version 2: 1 = rotate the key rows before quantising, 0 = not */
 } qsa_prep_args;
 
 /*

@@ -51,11 +51,11 @@ def qsa_score_workspace_bytes(ntok: int, head_dim: int = 128) -> int:
 
 
 def qsa_prep(q_in, k_in, v_in, norm_w, pos0, kq, vq, ksc, vsc, q_out, q_out_f32=None,
-             eps=1e-6, rope_theta=10000.0, rope_dims=64, stream=None):
+             eps=1e-6, rope_theta=10000.0, rope_dims=64, rope_k=False, stream=None):
     """Normalise + rotate q_in into q_out (fp16) / q_out_f32 and quantise k_in,
-    v_in into cache rows pos0 .. pos0+ntok-1.  Shapes: q_in [T, Hq, D] fp32,
-    k_in / v_in [T, 1, D] fp32, norm_w [D], kq / vq [C, D] int8, ksc / vsc
-    [C, D/32] fp16."""
+    v_in into cache rows pos0 .. pos0+ntok-1 (with rope_k, the key rows are
+    rotated first).  Shapes: q_in [T, Hq, D] fp32, k_in / v_in [T, 1, D]
+    fp32, norm_w [D], kq / vq [C, D] int8, ksc / vsc [C, D/32] fp16."""
     import torch
     T, H, D = q_in.shape
     a = _abi.PrepArgs(ntok=T, pos0=int(pos0), n_q_heads=H, n_kv_heads=k_in.shape[1], head_dim=D, group=32,
@@ -66,7 +66,8 @@ def qsa_prep(q_in, k_in, v_in, norm_w, pos0, kq, vq, ksc, vsc, q_out, q_out_f32=
                       q_out=_ptr(q_out, "q_out", torch.float16),
                       q_out_f32=_ptr(q_out_f32, "q_out_f32", torch.float32, optional=True),
                       kq=_ptr(kq, "kq", torch.int8), vq=_ptr(vq, "vq", torch.int8),
-                      ksc=_ptr(ksc, "ksc", torch.float16), vsc=_ptr(vsc, "vsc", torch.float16))
+                      ksc=_ptr(ksc, "ksc", torch.float16), vsc=_ptr(vsc, "vsc", torch.float16),
+                      rope_k=1 if rope_k else 0)
     _abi.check(lib().qsa_prep(ctypes.byref(a), _stream(stream)))
 
 

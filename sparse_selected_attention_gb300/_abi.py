@@ -27,7 +27,8 @@ class PrepArgs(ctypes.Structure):
                 ("head_dim", _c_int), ("group", _c_int), ("rope_dims", _c_int), ("cache_cells", _c_int),
                 ("eps", _c_float), ("rope_theta", _c_float),
                 ("q_in", _vp), ("k_in", _vp), ("v_in", _vp), ("norm_w", _vp),
-                ("q_out", _vp), ("q_out_f32", _vp), ("kq", _vp), ("vq", _vp), ("ksc", _vp), ("vsc", _vp)]
+                ("q_out", _vp), ("q_out_f32", _vp), ("kq", _vp), ("vq", _vp), ("ksc", _vp), ("vsc", _vp),
+                ("rope_k", _c_int)]
 
 
 class ScoreArgs(ctypes.Structure):

@@ -68,6 +68,7 @@ qsa_status qsa_prep(const qsa_prep_args *a, void *stream) {
     if ((long long)a->pos0 + a->ntok > kMaxPos) return fail(QSA_ERR_INVALID_ARG, "qsa_prep: positions beyond 2^29");
     if (!(a->eps >= 0.0f) || !std::isfinite(a->eps) || !(a->rope_theta > 0.0f) || !std::isfinite(a->rope_theta))
         return fail(QSA_ERR_INVALID_ARG, "qsa_prep: eps must be finite >= 0 and rope_theta finite > 0");
+    if (a->rope_k != 0 && a->rope_k != 1) return fail(QSA_ERR_INVALID_ARG, "qsa_prep: rope_k must be 0 or 1");
     if (a->ntok == 0) return QSA_OK;
     if (!a->q_in || !a->k_in || !a->v_in || !a->norm_w || !a->q_out || !a->kq || !a->vq || !a->ksc || !a->vsc)
         return fail(QSA_ERR_INVALID_ARG, "qsa_prep: NULL buffer");
@@ -82,6 +83,7 @@ qsa_status qsa_prep(const qsa_prep_args *a, void *stream) {
     L.rope_dims = a->rope_dims;
     L.eps = a->eps;
     L.rope_theta = a->rope_theta;
+    L.rope_k = a->rope_k;
     L.q_in = a->q_in;
     L.k_in = a->k_in;
     L.v_in = a->v_in;

@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepParams P) {
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ float2 cs[D / 2];
+    __shared__ float2 kcs[D / 2];  // fp32 of double-precision (cos, sin), for the key rotation
     const int half = a.rope_dims >> 1;
 
     // Issue this warp's row loads before the angle table is built.
@@ -64,6 +65,11 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepParams P) {
         float s, c;
         sincosf(r, &s, &c);
         cs[i] = make_float2(c, s);
+        if (a.rope_k) {
+            double sd, cd;
+            sincos(ang, &sd, &cd);
+            kcs[i] = make_float2((float)cd, (float)sd);
+        }
     }
     __syncthreads();
 
@@ -105,12 +111,38 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepParams P) {
     } else if (is_kv) {
         int8_t *dst = (is_v ? a.vq : a.kq) + (size_t)(a.pos0 + t) * D;
         uint16_t *sdst = (is_v ? a.vsc : a.ksc) + (size_t)(a.pos0 + t) * (D / G);
-        float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+        float xv[4] = {x.x, x.y, x.z, x.w};
+        if (a.rope_k && !is_v && half > 0) {
+            // Key rotation in explicit round-to-nearest fp32 steps (no fused
+            // multiply-add), the order the oracle defines, since the rotated
+            // values decide the codes.
+            const int sh = half >> 2;
+            float up[4], dn[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                up[e] = __shfl_down_sync(0xffffffffu, xv[e], sh);
+                dn[e] = __shfl_up_sync(0xffffffffu, xv[e], sh);
+            }
+            const int i0 = lane * 4;
+            if (i0 < half) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 c = kcs[i0 + e];
+                    xv[e] = __fsub_rn(__fmul_rn(xv[e], c.x), __fmul_rn(up[e], c.y));
+                }
+            } else if (i0 < 2 * half) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 c = kcs[i0 - half + e];
+                    xv[e] = __fadd_rn(__fmul_rn(xv[e], c.x), __fmul_rn(dn[e], c.y));
+                }
+            }
+        }
+        float amax = fmaxf(fmaxf(fabsf(xv[0]), fabsf(xv[1])), fmaxf(fabsf(xv[2]), fabsf(xv[3])));
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         const __half sh = __float2half_rn(__fdiv_rn(amax, 127.0f));
         const float sf = __half2float(sh);
-        const float xv[4] = {x.x, x.y, x.z, x.w};
         uint32_t packed = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {

@@ -17,6 +17,7 @@ struct PrepLaunch {
     float *q_out_f32;
     int8_t *kq, *vq;
     uint16_t *ksc, *vsc;
+    int rope_k;  // rotate the key rows (same pairs and angles as the queries) before quantising
 };
 
 struct ScoreLaunch {

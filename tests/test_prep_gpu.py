@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 Q32_ATOL = 2e-5   # fp32 arithmetic on O(1) values: a few ulp of the row scale
 
 
-def run_case(T, pos0, rope_dims=64, heads=12, extra=7, seed=41):
+def run_case(T, pos0, rope_dims=64, heads=12, extra=7, seed=41, rope_k=False):
     inp = wl.prep_inputs(T, seed=seed, heads=heads)
     C = pos0 + T + extra
     cache = wl.make_cache(C, seed=seed)
@@ -26,11 +26,11 @@ def run_case(T, pos0, rope_dims=64, heads=12, extra=7, seed=41):
     q_out = torch.full((T, heads, 128), float("nan"), dtype=torch.float16, device="cuda")
     q32 = torch.full((T, heads, 128), float("nan"), dtype=torch.float32, device="cuda")
     qsa_prep(dev(inp.q_in), dev(inp.k_in), dev(inp.v_in), dev(inp.norm_w), pos0, kq, vq, ksc, vsc, q_out,
-             q_out_f32=q32, rope_dims=rope_dims)
+             q_out_f32=q32, rope_dims=rope_dims, rope_k=rope_k)
     torch.cuda.synchronize()
     ref_cache = cache.copy()
     q64, _, _ = oracle_prep(inp.q_in, inp.k_in, inp.v_in, inp.norm_w, pos0, ref_cache.kq, ref_cache.vq,
-                            ref_cache.ksc, ref_cache.vsc, rope_dims=rope_dims)
+                            ref_cache.ksc, ref_cache.vsc, rope_dims=rope_dims, rope_k=rope_k)
     assert_f16_close(q_out.cpu(), q64, f"q fp16 T={T} pos0={pos0}")
     np.testing.assert_allclose(q32.cpu().numpy(), q64, atol=Q32_ATOL, rtol=0)
     for name, g, r in (("kq", kq, ref_cache.kq), ("vq", vq, ref_cache.vq),
@@ -70,3 +70,11 @@ def test_prep_zero_group_and_large_values(cuda_device):
     assert np.array_equal(ksc.cpu().numpy().view(np.int16), ref.ksc.view(np.int16))
     assert np.array_equal(vsc.cpu().numpy().view(np.int16), ref.vsc.view(np.int16))
     assert float(ref.ksc[pos0, 1]) == 0.0 and float(ref.vsc[pos0 + 2, 3]) == 0.0
+
+
+@pytest.mark.parametrize("T,pos0,rope_dims", [(1984, 30000, 64), (64, 0, 64), (19, 1234, 8), (19, 1234, 128),
+                                              (300, 32000, 64)])
+def test_prep_rope_k(cuda_device, T, pos0, rope_dims):
+    """Key rotation before quantisation: codes and scale bits bit-exact with
+    the oracle, at angles up to ~32 K rad."""
+    run_case(T, pos0, rope_dims=rope_dims, rope_k=True, seed=47)
