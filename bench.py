@@ -5,7 +5,9 @@ pos0 = 30000 over a 31984-cell int8 K/V cache (fp16 scales per 32 dims),
 12 query heads sharing one KV head, head_dim 128, 2048 evenly spaced causal
 selected ids per token (W = 2048).  The step normalises/rotates the queries
 and quantises the new K/V rows into the cache, scores every causal cell
-(fp32 queries, 61.5 M scores written) and runs the selected-id attention.
+(fp32 queries, 61.5 M scores written) and runs the selected-id attention;
+the score runs on a second stream beside the attention, since both depend
+only on prep.
 
 With --select the step also runs qsa_select between the score and the
 attention: each token keeps 64 sink cells, the previous 256 cells and its own
@@ -288,30 +290,40 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     names = KERNELS_SELECT if args.select else KERNELS
-    nk = len(names)
 
     main_bufs = {"q": q_in, "k": k_in, "v": v_in, "ids": ids, "out": out}
+    # Score and attention both depend only on prep, so without selection the
+    # score runs on a second stream beside the attention (it is bound by DRAM
+    # writes, the attention by instruction issue on an L2-resident cache);
+    # the step ends when both have.  With selection the chain is serial.
+    side = torch.cuda.Stream(dev)
+    ev_prep, ev_side = torch.cuda.Event(), torch.cuda.Event()
+
+    def timed(ev, name, st, fn):
+        if ev:
+            ev[name][0].record(st)
+        fn()
+        if ev:
+            ev[name][1].record(st)
 
     def step(ev=None, b=main_bufs):
-        i = 0
         if ev:
-            ev[i].record(stream)
-        qsa_prep(b["q"], b["k"], b["v"], norm_w, pos0, kq, vq, ksc, vsc, q16, q_out_f32=q32)
-        i += 1
-        if ev:
-            ev[i].record(stream)
-        qsa_score(q32, kq, ksc, pos0, scores, ws)
+            ev["step"][0].record(stream)
+        timed(ev, "prep", stream,
+              lambda: qsa_prep(b["q"], b["k"], b["v"], norm_w, pos0, kq, vq, ksc, vsc, q16, q_out_f32=q32))
         if args.select:
-            i += 1
-            if ev:
-                ev[i].record(stream)
-            qsa_select(scores, pos0, b["ids"])
-        i += 1
+            timed(ev, "score", stream, lambda: qsa_score(q32, kq, ksc, pos0, scores, ws))
+            timed(ev, "select", stream, lambda: qsa_select(scores, pos0, b["ids"]))
+            timed(ev, "attn", stream, lambda: qsa_attn(q16, kq, vq, ksc, vsc, b["ids"], b["out"]))
+        else:
+            ev_prep.record(stream)
+            side.wait_event(ev_prep)
+            timed(ev, "attn", stream, lambda: qsa_attn(q16, kq, vq, ksc, vsc, b["ids"], b["out"]))
+            timed(ev, "score", side, lambda: qsa_score(q32, kq, ksc, pos0, scores, ws, stream=side))
+            ev_side.record(side)
+            stream.wait_event(ev_side)
         if ev:
-            ev[i].record(stream)
-        qsa_attn(q16, kq, vq, ksc, vsc, b["ids"], b["out"])
-        if ev:
-            ev[i + 1].record(stream)
+            ev["step"][1].record(stream)
 
     def barrier():
         if world > 1:
@@ -324,7 +336,8 @@ def run_ours(args, rank, world, local_rank):
     barrier()
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(K)]
+    evs = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for n in names + ("step",)} for _ in range(K)]
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
@@ -336,8 +349,8 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
-    per = {n: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)] for i, n in enumerate(names)}
-    step_ms = [evs[k][0].elapsed_time(evs[k][nk]) for k in range(K)]
+    per = {n: [evs[k][n][0].elapsed_time(evs[k][n][1]) for k in range(K)] for n in names}
+    step_ms = [evs[k]["step"][0].elapsed_time(evs[k]["step"][1]) for k in range(K)]
     ms = max_over_ranks(sum(step_ms) / K, dev)
 
     # End to end through the public API, as a serving loop runs it: every
@@ -404,7 +417,10 @@ def run_ours(args, rank, world, local_rank):
 
     # Roofline of the dominant kernel.
     avg = {n: sum(v) / K for n, v in per.items()}
-    dom = max(avg, key=avg.get)
+    # Overlapped, the score's event window also spans its wait for SMs the
+    # attention holds; the attention (main stream, the step's critical path)
+    # is then the kernel whose own launch time bounds the step.
+    dom = max(avg, key=avg.get) if args.select else "attn"
     ab, valid = attn_bytes(ids.cpu().numpy() if args.select else ids_np, T)
     alg = {"attn": ab, "score": score_bytes(T, pos0, C), "prep": prep_bytes(T)}
     if args.select:
@@ -417,6 +433,8 @@ def run_ours(args, rank, world, local_rank):
     kernels = {n: {"avg_ms": avg[n], "algorithmic_bytes": alg[n],
                    "achieved_gbs": alg[n] / (avg[n] / 1e3) / 1e9} for n in names}
     kernels["score"]["pairs"] = score_pairs(T, pos0)
+    if not args.select:
+        kernels["score"]["overlapped_with"] = "attn (second stream; the window includes waiting for SMs)"
     kernels["score"]["tflops_algorithmic"] = 2 * HQ * D * score_pairs(T, pos0) / (avg["score"] / 1e3) / 1e12
     kernels["attn"]["valid_cells"] = valid
     return {"ms": ms, "wall_s": wall, "e2e": e2e, "clocks": clocks, "roofline": roof, "kernels": kernels,
