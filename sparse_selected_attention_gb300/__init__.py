@@ -16,10 +16,12 @@ import ctypes
 import math
 
 from . import _abi
-from ._abi import (QSA_DEVERR_BAD_ID, QSA_DEVERR_TIMEOUT, QSAError, lib)  # noqa: F401
+from ._abi import (QSA_DEVERR_BAD_ID, QSA_DEVERR_TIMEOUT, QSA_SCORE_NOALLOC_MAX_TOKENS,  # noqa: F401
+                   QSA_SELECT_MAX_CELLS, QSAError, lib)
 
 __all__ = ["qsa_prep", "qsa_score", "qsa_score_noalloc", "qsa_select", "qsa_attn", "qsa_score_workspace_bytes", "qsa_abi_version",
-           "QSAError", "QSA_DEVERR_BAD_ID", "QSA_DEVERR_TIMEOUT", "lib"]
+           "QSAError", "QSA_DEVERR_BAD_ID", "QSA_DEVERR_TIMEOUT", "QSA_SCORE_NOALLOC_MAX_TOKENS",
+           "QSA_SELECT_MAX_CELLS", "lib"]
 
 
 def _ptr(t, name, dtype=None, optional=False):
