@@ -51,6 +51,7 @@ constexpr int UNIT = 32;   // cells per warp step
 constexpr int CHUNK = 64;  // cells per chunk of the definition
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr float RESCALE_SLACK = 8.0f;  // fused path: probabilities below 2^8 (exact in fp16 range)
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
@@ -451,7 +452,12 @@ __device__ __forceinline__ void compute_staged(const uint8_t *stp, unsigned vmas
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
     }
-    const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+    // Lazy rescale: the reference maximum moves only when a unit's maximum
+    // exceeds it by more than RESCALE_SLACK (base-2 logits), so the
+    // probabilities stay below 2^RESCALE_SLACK and the values are rarely
+    // rescaled; the max-first merge only needs a consistent reference.
+    const float mn0 = mx0 > st.m[0] + RESCALE_SLACK ? mx0 : st.m[0];
+    const float mn1 = mx1 > st.m[1] + RESCALE_SLACK ? mx1 : st.m[1];
     const float al0 = exp2f(st.m[0] - mn0), al1 = exp2f(st.m[1] - mn1);
     st.m[0] = mn0;
     st.m[1] = mn1;
