@@ -5,7 +5,8 @@ pos0 = 30000 over a 31984-cell int8 K/V cache (fp16 scales per 32 dims),
 12 query heads sharing one KV head, head_dim 128, 2048 evenly spaced causal
 selected ids per token (W = 2048).  The step normalises/rotates the queries
 and quantises the new K/V rows into the cache, scores every causal cell
-(fp32 queries, 61.5 M scores written) and runs the selected-id attention;
+(from the head sum of the rotated fp32 queries, which prep writes into the
+score's workspace; 61.5 M scores written) and runs the selected-id attention;
 the score runs on a second stream beside the attention, since both depend
 only on prep.
 
@@ -40,7 +41,8 @@ UNIT = "tokens/s"
 NTOK, POS0, WIDTH, HQ, D, G = 1984, 30000, 2048, 12, 128, 32
 WORKLOAD = ("prompt attention long context: T=1984 query tokens, pos0=30000, int8 K/V cache of 31984 cells "
             "with fp16 per-32 scales, 12 q heads / 1 KV head, head_dim 128, 2048 evenly spaced causal ids per "
-            "token; step = qsa_prep + qsa_score (fp32 q, all causal cells) + qsa_attn")
+            "token; step = qsa_prep + qsa_score (all causal cells, from the head sum of the fp32 rotated queries that "
+            "qsa_prep writes) + qsa_attn")
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 KERNELS = ("prep", "score", "attn")
@@ -86,9 +88,11 @@ def score_pairs(ntok, pos0):
 
 
 def score_bytes(ntok, pos0, cells):
-    """fp32 q read, int8 codes + fp16 scales of every cell read, one fp32 score
-    written per causal (token, cell) pair."""
-    return ntok * HQ * D * 4 + cells * (D + 2 * (D // G)) + 4 * score_pairs(ntok, pos0)
+    """The head sum read (fp16 hi/lo rows, prep writes it), int8 codes + fp16
+    scales of every cell read, one fp32 score written per causal (token, cell)
+    pair."""
+    ntok_pad = -(-ntok // 64) * 64
+    return ntok_pad * 2 * D * 2 + cells * (D + 2 * (D // G)) + 4 * score_pairs(ntok, pos0)
 
 
 def select_bytes(ntok, pos0, sink=64, local=256):
@@ -100,7 +104,11 @@ def select_bytes(ntok, pos0, sink=64, local=256):
 
 
 def prep_bytes(ntok):
-    return ntok * HQ * D * (4 + 2 + 4) + 2 * ntok * D * 4 + 2 * ntok * (D + 2 * (D // G)) + D * 4
+    """fp32 q, k, v rows read, fp16 q written, int8 K/V codes and fp16 scales
+    written, the score's head sum (fp16 hi/lo rows) written, the norm weight."""
+    ntok_pad = -(-ntok // 64) * 64
+    return (ntok * HQ * D * (4 + 2) + 2 * ntok * D * 4 + 2 * ntok * (D + 2 * (D // G)) + ntok_pad * 2 * D * 2
+            + D * 4)
 
 
 def peaks():
@@ -282,7 +290,6 @@ def run_ours(args, rank, world, local_rank):
     kq, vq, ksc, vsc = d(cache.kq), d(cache.vq), d(cache.ksc), d(cache.vsc)
     ids = d(ids_np)
     q16 = torch.empty((T, HQ, D), dtype=torch.float16, device=dev)
-    q32 = torch.empty((T, HQ, D), dtype=torch.float32, device=dev)
     scores = torch.empty((T, C), dtype=torch.float32, device=dev)
     ws = torch.empty(qsa_score_workspace_bytes(T), dtype=torch.uint8, device=dev)
     out = torch.empty((T, HQ, D), dtype=torch.float16, device=dev)
@@ -310,9 +317,10 @@ def run_ours(args, rank, world, local_rank):
         if ev:
             ev["step"][0].record(stream)
         timed(ev, "prep", stream,
-              lambda: qsa_prep(b["q"], b["k"], b["v"], norm_w, pos0, kq, vq, ksc, vsc, q16, q_out_f32=q32))
+              lambda: qsa_prep(b["q"], b["k"], b["v"], norm_w, pos0, kq, vq, ksc, vsc, q16, qbar_out=ws))
         if args.select or serial:
-            timed(ev, "score", stream, lambda: qsa_score(q32, kq, ksc, pos0, scores, ws))
+            timed(ev, "score", stream,
+                  lambda: qsa_score(None, kq, ksc, pos0, scores, ws, workspace_holds_qbar=True))
             if args.select:
                 timed(ev, "select", stream, lambda: qsa_select(scores, pos0, b["ids"]))
             timed(ev, "attn", stream, lambda: qsa_attn(q16, kq, vq, ksc, vsc, b["ids"], b["out"]))
@@ -320,7 +328,8 @@ def run_ours(args, rank, world, local_rank):
             ev_prep.record(stream)
             side.wait_event(ev_prep)
             timed(ev, "attn", stream, lambda: qsa_attn(q16, kq, vq, ksc, vsc, b["ids"], b["out"]))
-            timed(ev, "score", side, lambda: qsa_score(q32, kq, ksc, pos0, scores, ws, stream=side))
+            timed(ev, "score", side,
+                  lambda: qsa_score(None, kq, ksc, pos0, scores, ws, stream=side, workspace_holds_qbar=True))
             ev_side.record(side)
             stream.wait_event(ev_side)
         if ev:
@@ -453,7 +462,7 @@ def run_ours(args, rank, world, local_rank):
     kernels["score"]["tflops_algorithmic"] = 2 * HQ * D * score_pairs(T, pos0) / (own["score"] / 1e3) / 1e12
     kernels["attn"]["valid_cells"] = valid
     return {"ms": ms, "wall_s": wall, "e2e": e2e, "clocks": clocks, "roofline": roof, "kernels": kernels,
-            "launches_per_step": 5 if args.select else 4}
+            "launches_per_step": 4 if args.select else 3}  # prep, score, (select,) attention
 
 
 def run_pages(args, rank, world, local_rank):

@@ -72,6 +72,13 @@ typedef enum { QSA_F32 = 0, QSA_F16 = 1 } qsa_dtype;
  * double-precision cos / sin, k'[i] = fp32(fp32(k[i] c) - fp32(k[i+h] s)),
  * k'[i+h] = fp32(fp32(k[i+h] c) + fp32(k[i] s)); the pages rotate only the
  * query rows, so this is an option (off = 0).
+ * qbar_out: NULL, or a qsa_score workspace for these ntok tokens (at least
+ * qsa_score_workspace_bytes(ntok, head_dim) bytes, 256-byte aligned) that
+ * receives the score's head sum of the rotated queries: per token, fp32
+ * qbar[d] = sum_h q_out_f32[t,h,d] in head order, stored as the fp16 pair
+ * hi = fp16(qbar), lo = fp16(qbar - hi), padding rows zero.  A following
+ * qsa_score with workspace_holds_qbar = 1 then needs neither q nor its own
+ * head-sum pass.
  *
  * Layouts (row-major, contiguous): q_in [ntok, n_q_heads, head_dim] fp32;
  * k_in, v_in [ntok, n_kv_heads, head_dim] fp32; norm_w [head_dim] fp32;
@@ -90,6 +97,7 @@ typedef struct {
     int8_t *kq, *vq;
     uint16_t *ksc, *vsc;
     int rope_k; /* added in ABI version 2: 1 = rotate the key rows before quantising, 0 = not */
+    void *qbar_out; /* added in ABI version 2: NULL or a qsa_score workspace, see above */
 } qsa_prep_args;
 
 /*
@@ -107,7 +115,11 @@ typedef struct {
  * scores: fp32, row stride ld (elements), ld >= pos0 + ntok.
  * workspace: device scratch of at least qsa_score_workspace_bytes(ntok,
  * head_dim) bytes, 256-byte aligned; the call overwrites it.  Two calls that
- * share a workspace must not run concurrently.
+ * share a workspace must not run concurrently.  It holds the head sum the
+ * score is computed from: with workspace_holds_qbar = 1 the caller has
+ * already filled it through qsa_prep's qbar_out for the same tokens, q is
+ * ignored (it may be NULL) and the head-sum pass is skipped; the scores are
+ * bit-identical to those computed from the fp32 q_out_f32 of that prep.
  * Requires pos0 + ntok <= cache_cells.  Supported: head_dim == 128,
  * group == 32, 1 <= n_q_heads <= 64.  q, kq 16-byte aligned; ksc 8-byte.
  */
@@ -122,6 +134,7 @@ typedef struct {
     void *workspace;
     size_t workspace_bytes;
     unsigned int *err;
+    int workspace_holds_qbar; /* added in ABI version 2: 0 or 1, see above */
 } qsa_score_args;
 
 /* Bytes of workspace qsa_score needs for `ntok` tokens (0 on bad input). */
@@ -186,7 +199,8 @@ typedef struct {
  * the caller's workspace it uses a scratch array built into the library
  * (QSA_SCORE_NOALLOC_MAX_TOKENS * 512 bytes = 4 MiB of device memory, held on
  * every GPU that loads the library until the process exits).  The
- * `workspace` and `workspace_bytes` fields are ignored.
+ * `workspace`, `workspace_bytes` and `workspace_holds_qbar` fields are ignored:
+ * the head sum is always computed from q.
  *
  *  - ntok above QSA_SCORE_NOALLOC_MAX_TOKENS is rejected with
  *    QSA_ERR_INVALID_ARG; nothing is enqueued.

@@ -53,11 +53,14 @@ def qsa_score_workspace_bytes(ntok: int, head_dim: int = 128) -> int:
 
 
 def qsa_prep(q_in, k_in, v_in, norm_w, pos0, kq, vq, ksc, vsc, q_out, q_out_f32=None,
-             eps=1e-6, rope_theta=10000.0, rope_dims=64, rope_k=False, stream=None):
+             eps=1e-6, rope_theta=10000.0, rope_dims=64, rope_k=False, qbar_out=None, stream=None):
     """Normalise + rotate q_in into q_out (fp16) / q_out_f32 and quantise k_in,
     v_in into cache rows pos0 .. pos0+ntok-1 (with rope_k, the key rows are
     rotated first).  Shapes: q_in [T, Hq, D] fp32, k_in / v_in [T, 1, D]
-    fp32, norm_w [D], kq / vq [C, D] int8, ksc / vsc [C, D/32] fp16."""
+    fp32, norm_w [D], kq / vq [C, D] int8, ksc / vsc [C, D/32] fp16.
+    qbar_out, if given, is a qsa_score workspace (qsa_score_workspace_bytes(T)
+    bytes) that receives the score's head sum, for a qsa_score call with
+    workspace_holds_qbar=True."""
     import torch
     T, H, D = q_in.shape
     a = _abi.PrepArgs(ntok=T, pos0=int(pos0), n_q_heads=H, n_kv_heads=k_in.shape[1], head_dim=D, group=32,
@@ -69,22 +72,32 @@ def qsa_prep(q_in, k_in, v_in, norm_w, pos0, kq, vq, ksc, vsc, q_out, q_out_f32=
                       q_out_f32=_ptr(q_out_f32, "q_out_f32", torch.float32, optional=True),
                       kq=_ptr(kq, "kq", torch.int8), vq=_ptr(vq, "vq", torch.int8),
                       ksc=_ptr(ksc, "ksc", torch.float16), vsc=_ptr(vsc, "vsc", torch.float16),
-                      rope_k=1 if rope_k else 0)
+                      rope_k=1 if rope_k else 0, qbar_out=_ptr(qbar_out, "qbar_out", optional=True))
     _abi.check(lib().qsa_prep(ctypes.byref(a), _stream(stream)))
 
 
-def qsa_score(q, kq, ksc, pos0, scores, workspace, err=None, stream=None):
+def qsa_score(q, kq, ksc, pos0, scores, workspace, err=None, stream=None, workspace_holds_qbar=False,
+              n_q_heads=12):
     """scores[t, c] for c <= pos0 + t (others untouched).  q [T, Hq, D] fp32 or
     fp16; scores [T, ld] fp32 with ld >= pos0 + T; workspace a uint8 CUDA
-    tensor of at least qsa_score_workspace_bytes(T) bytes."""
+    tensor of at least qsa_score_workspace_bytes(T) bytes.  With
+    workspace_holds_qbar=True the workspace was filled by qsa_prep(qbar_out=)
+    for these tokens and q may be None (T is then scores.shape[0])."""
     import torch
-    T, H, D = q.shape
-    if q.dtype not in (torch.float32, torch.float16):
-        raise ValueError("q must be float32 or float16")
+    if q is None:
+        if not workspace_holds_qbar:
+            raise ValueError("q is required unless the workspace holds the head sum")
+        T, H, D = scores.shape[0], int(n_q_heads), 128
+        qp, qdt = None, _abi.QSA_F32
+    else:
+        T, H, D = q.shape
+        if q.dtype not in (torch.float32, torch.float16):
+            raise ValueError("q must be float32 or float16")
+        qp, qdt = _ptr(q, "q"), (_abi.QSA_F16 if q.dtype == torch.float16 else _abi.QSA_F32)
     if scores.dim() != 2 or scores.shape[0] < T:
         raise ValueError("scores must be [T, ld]")
     a = _abi.ScoreArgs(ntok=T, pos0=int(pos0), n_q_heads=H, head_dim=D, group=32, cache_cells=kq.shape[0],
-                       q=_ptr(q, "q"), q_dtype=_abi.QSA_F16 if q.dtype == torch.float16 else _abi.QSA_F32,
+                       q=qp, q_dtype=qdt, workspace_holds_qbar=1 if workspace_holds_qbar else 0,
                        kq=_ptr(kq, "kq", torch.int8), ksc=_ptr(ksc, "ksc", torch.float16),
                        scores=_ptr(scores, "scores", torch.float32), ld=scores.shape[1],
                        workspace=_ptr(workspace, "workspace"),

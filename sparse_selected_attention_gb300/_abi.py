@@ -28,14 +28,15 @@ class PrepArgs(ctypes.Structure):
                 ("eps", _c_float), ("rope_theta", _c_float),
                 ("q_in", _vp), ("k_in", _vp), ("v_in", _vp), ("norm_w", _vp),
                 ("q_out", _vp), ("q_out_f32", _vp), ("kq", _vp), ("vq", _vp), ("ksc", _vp), ("vsc", _vp),
-                ("rope_k", _c_int)]
+                ("rope_k", _c_int), ("qbar_out", _vp)]
 
 
 class ScoreArgs(ctypes.Structure):
     _fields_ = [("ntok", _c_int), ("pos0", _c_int), ("n_q_heads", _c_int), ("head_dim", _c_int),
                 ("group", _c_int), ("cache_cells", _c_int),
                 ("q", _vp), ("q_dtype", _c_int), ("kq", _vp), ("ksc", _vp), ("scores", _vp),
-                ("ld", ctypes.c_int64), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("err", _vp)]
+                ("ld", ctypes.c_int64), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("err", _vp),
+                ("workspace_holds_qbar", _c_int)]
 
 
 class SelectArgs(ctypes.Structure):

@@ -69,6 +69,7 @@ qsa_status qsa_prep(const qsa_prep_args *a, void *stream) {
     if (!(a->eps >= 0.0f) || !std::isfinite(a->eps) || !(a->rope_theta > 0.0f) || !std::isfinite(a->rope_theta))
         return fail(QSA_ERR_INVALID_ARG, "qsa_prep: eps must be finite >= 0 and rope_theta finite > 0");
     if (a->rope_k != 0 && a->rope_k != 1) return fail(QSA_ERR_INVALID_ARG, "qsa_prep: rope_k must be 0 or 1");
+    if (a->qbar_out && !aligned(a->qbar_out, 256)) return fail(QSA_ERR_INVALID_ARG, "qsa_prep: misaligned qbar_out");
     if (a->ntok == 0) return QSA_OK;
     if (!a->q_in || !a->k_in || !a->v_in || !a->norm_w || !a->q_out || !a->kq || !a->vq || !a->ksc || !a->vsc)
         return fail(QSA_ERR_INVALID_ARG, "qsa_prep: NULL buffer");
@@ -84,6 +85,8 @@ qsa_status qsa_prep(const qsa_prep_args *a, void *stream) {
     L.eps = a->eps;
     L.rope_theta = a->rope_theta;
     L.rope_k = a->rope_k;
+    L.qbar = static_cast<uint16_t *>(a->qbar_out);
+    L.ntok_pad = (a->ntok + 63) / 64 * 64;
     L.q_in = a->q_in;
     L.k_in = a->k_in;
     L.v_in = a->v_in;
@@ -108,17 +111,20 @@ qsa_status qsa_score(const qsa_score_args *a, void *stream) {
     if ((long long)a->pos0 + a->ntok > a->cache_cells)
         return fail(QSA_ERR_INVALID_ARG, "qsa_score: pos0 + ntok exceeds cache_cells");
     if (a->ld < (long long)a->pos0 + a->ntok) return fail(QSA_ERR_INVALID_ARG, "qsa_score: ld < pos0 + ntok");
+    if (a->workspace_holds_qbar != 0 && a->workspace_holds_qbar != 1)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_score: workspace_holds_qbar must be 0 or 1");
     if (a->ntok == 0) return QSA_OK;
-    if (!a->q || !a->kq || !a->ksc || !a->scores || !a->workspace)
+    const bool need_q = !a->workspace_holds_qbar;
+    if ((need_q && !a->q) || !a->kq || !a->ksc || !a->scores || !a->workspace)
         return fail(QSA_ERR_INVALID_ARG, "qsa_score: NULL buffer");
     if (a->workspace_bytes < qsa_score_workspace_bytes(a->ntok, a->head_dim))
         return fail(QSA_ERR_INVALID_ARG, "qsa_score: workspace smaller than qsa_score_workspace_bytes()");
-    if (!aligned(a->q, 16) || !aligned(a->kq, 16) || !aligned(a->ksc, 8) || !aligned(a->scores, 4) ||
+    if ((need_q && !aligned(a->q, 16)) || !aligned(a->kq, 16) || !aligned(a->ksc, 8) || !aligned(a->scores, 4) ||
         !aligned(a->workspace, 256))
         return fail(QSA_ERR_INVALID_ARG, "qsa_score: misaligned buffer");
     qsa::ScoreLaunch L{a->ntok,   a->pos0, a->n_q_heads, a->cache_cells, a->q, a->q_dtype == QSA_F16 ? 1 : 0,
                        a->kq,     a->ksc,  a->scores,    a->ld,          static_cast<uint16_t *>(a->workspace),
-                       a->err};
+                       a->err,    a->workspace_holds_qbar};
     cudaError_t e = qsa::launch_score(L, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_score");
 }

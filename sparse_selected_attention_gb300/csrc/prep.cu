@@ -36,10 +36,17 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+constexpr int MAXQH = 30;  // query heads per token (the launcher's limit)
+
 __global__ void __launch_bounds__(1024) prep_kernel(PrepParams P) {
     const PrepLaunch &a = P.a;
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (t >= a.ntok) {  // padding rows of the score's head sum
+        for (int i = threadIdx.x; i < 2 * D; i += blockDim.x) a.qbar[(size_t)t * 2 * D + i] = 0;
+        return;
+    }
+    __shared__ float4 qrows[MAXQH][D / 4];  // rotated query rows, for the head sum
     __shared__ float2 cs[D / 2];
     __shared__ float2 kcs[D / 2];  // fp32 of double-precision (cos, sin), for the key rotation
     const int half = a.rope_dims >> 1;
@@ -101,6 +108,7 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepParams P) {
                 }
             }
         }
+        if (a.qbar) qrows[warp][lane] = make_float4(y[0], y[1], y[2], y[3]);
         const __half2 h01 = __floats2half2_rn(y[0], y[1]);
         const __half2 h23 = __floats2half2_rn(y[2], y[3]);
         uint2 hv;
@@ -153,6 +161,20 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepParams P) {
         reinterpret_cast<uint32_t *>(dst)[lane] = packed;
         if ((lane & 7) == 0) sdst[lane >> 3] = __half_as_ushort(sh);
     }
+    if (a.qbar) {
+        // The score's head sum: fp32, heads in order (as the score's own
+        // head-sum pass adds the fp32 rows), split into an fp16 hi/lo pair.
+        __syncthreads();
+        for (int d = threadIdx.x; d < D; d += blockDim.x) {
+            const float *rows = reinterpret_cast<const float *>(qrows);
+            float sum = 0.0f;
+            for (int h = 0; h < a.n_q_heads; ++h) sum += rows[h * D + d];
+            const __half hi = __float2half_rn(sum);
+            const __half lo = __float2half_rn(sum - __half2float(hi));
+            a.qbar[(size_t)t * 2 * D + d] = __half_as_ushort(hi);
+            a.qbar[(size_t)t * 2 * D + D + d] = __half_as_ushort(lo);
+        }
+    }
 }
 
 }  // namespace
@@ -163,7 +185,7 @@ cudaError_t launch_prep(const PrepLaunch &a, cudaStream_t s) {
     for (int i = 0; i < a.rope_dims / 2; ++i)
         P.a.inv_freq[i] = (float)std::pow((double)a.rope_theta, -2.0 * (double)i / (double)a.rope_dims);
     const int threads = 32 * (a.n_q_heads + 2);
-    prep_kernel<<<a.ntok, threads, 0, s>>>(P);
+    prep_kernel<<<a.qbar ? a.ntok_pad : a.ntok, threads, 0, s>>>(P);
     return cudaGetLastError();
 }
 

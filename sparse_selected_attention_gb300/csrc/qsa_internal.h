@@ -18,6 +18,8 @@ struct PrepLaunch {
     int8_t *kq, *vq;
     uint16_t *ksc, *vsc;
     int rope_k;  // rotate the key rows (same pairs and angles as the queries) before quantising
+    uint16_t *qbar;  // NULL or [ntok_pad, 2, 128] fp16: the score's head sum (hi row, lo row)
+    int ntok_pad;    // ntok rounded up to 64 (rows of qbar)
 };
 
 struct ScoreLaunch {
@@ -30,6 +32,7 @@ struct ScoreLaunch {
     int64_t ld;
     uint16_t *qsum;  // workspace: [ntok_pad, 2, 128] fp16 (hi row, lo row)
     unsigned int *err;
+    int qsum_ready;  // the workspace already holds the head sum (written by prep)
 };
 
 struct AttnLaunch {

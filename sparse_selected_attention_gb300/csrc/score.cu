@@ -414,10 +414,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 cudaError_t launch_score(const ScoreLaunch &a, cudaStream_t s) {
     if (a.ntok == 0) return cudaSuccess;
     const int ntok_pad = (a.ntok + TN - 1) / TN * TN;
-    if (a.q_f16)
-        qsum_kernel<true><<<ntok_pad, D, 0, s>>>(a);
-    else
-        qsum_kernel<false><<<ntok_pad, D, 0, s>>>(a);
+    if (!a.qsum_ready) {  // otherwise qsa_prep has written the head sum into the workspace
+        if (a.q_f16)
+            qsum_kernel<true><<<ntok_pad, D, 0, s>>>(a);
+        else
+            qsum_kernel<false><<<ntok_pad, D, 0, s>>>(a);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;

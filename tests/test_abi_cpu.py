@@ -154,3 +154,16 @@ def _select(**kw):
 def test_select_rejects(L, kw, want):
     s, msg = _status(L, "qsa_select", _select(**kw))
     assert s == want and msg.startswith("qsa_select")
+
+
+def test_score_and_prep_head_sum_flags_rejected(L):
+    a = _abi.ScoreArgs(ntok=4, pos0=10, n_q_heads=12, head_dim=128, group=32, cache_cells=100, q=FAKE, q_dtype=0,
+                       kq=FAKE, ksc=FAKE, scores=FAKE, ld=20, workspace=FAKE, workspace_bytes=1 << 20, err=None,
+                       workspace_holds_qbar=2)
+    s, msg = _status(L, "qsa_score", a)
+    assert s == _abi.QSA_ERR_INVALID_ARG and "workspace_holds_qbar" in msg
+    p = _abi.PrepArgs(ntok=4, pos0=10, n_q_heads=12, n_kv_heads=1, head_dim=128, group=32, rope_dims=64,
+                      cache_cells=100, eps=1e-6, rope_theta=1e4, q_in=FAKE, k_in=FAKE, v_in=FAKE, norm_w=FAKE,
+                      q_out=FAKE, q_out_f32=None, kq=FAKE, vq=FAKE, ksc=FAKE, vsc=FAKE, rope_k=0, qbar_out=FAKE + 16)
+    s, msg = _status(L, "qsa_prep", p)
+    assert s == _abi.QSA_ERR_INVALID_ARG and "qbar_out" in msg

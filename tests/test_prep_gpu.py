@@ -78,3 +78,28 @@ def test_prep_rope_k(cuda_device, T, pos0, rope_dims):
     """Key rotation before quantisation: codes and scale bits bit-exact with
     the oracle, at angles up to ~32 K rad."""
     run_case(T, pos0, rope_dims=rope_dims, rope_k=True, seed=47)
+
+
+@pytest.mark.parametrize("T,heads", [(150, 12), (64, 1), (1, 30)])
+def test_prep_head_sum_feeds_the_score(cuda_device, T, heads):
+    """qsa_prep's qbar_out is the score's own head sum bit for bit, and a
+    score from it equals the score from q_out_f32 bit for bit."""
+    from sparse_selected_attention_gb300 import qsa_score, qsa_score_workspace_bytes
+    pos0 = 3000
+    inp = wl.prep_inputs(T, seed=48, heads=heads)
+    cache = wl.make_cache(pos0 + T, seed=48)
+    kq, vq, ksc, vsc = dev(cache.kq), dev(cache.vq), dev(cache.ksc), dev(cache.vsc)
+    q16 = torch.empty((T, heads, 128), dtype=torch.float16, device="cuda")
+    q32 = torch.empty((T, heads, 128), dtype=torch.float32, device="cuda")
+    nb = qsa_score_workspace_bytes(T)
+    ws_prep = torch.full((nb,), 0x7f, dtype=torch.uint8, device="cuda")
+    ws_score = torch.full((nb,), 0x55, dtype=torch.uint8, device="cuda")
+    qsa_prep(dev(inp.q_in), dev(inp.k_in), dev(inp.v_in), dev(inp.norm_w), pos0, kq, vq, ksc, vsc, q16,
+             q_out_f32=q32, qbar_out=ws_prep)
+    s_q = torch.full((T, pos0 + T), -1, dtype=torch.int32, device="cuda").view(torch.float32)
+    s_bar = s_q.clone()
+    qsa_score(q32, kq, ksc, pos0, s_q, ws_score)
+    qsa_score(None, kq, ksc, pos0, s_bar, ws_prep, workspace_holds_qbar=True, n_q_heads=heads)
+    torch.cuda.synchronize()
+    assert torch.equal(ws_prep, ws_score)                    # padding rows included
+    assert torch.equal(s_q.view(torch.int32), s_bar.view(torch.int32))
