@@ -49,3 +49,41 @@ def assert_score_close(gpu_rows, ref, A, what=""):
                              f"ref={ref[i]} A={A[i]}")
     rel = np.where(causal, err / np.maximum(A, 1e-300), 0.0)
     return float(rel.max()) if rel.size else 0.0
+
+
+def assert_valid_selection(got, ref_ids, S, A, pos0, budget=2048, sink=64, local=256, what=""):
+    """Selection made by the GPU from its own scores, judged against the
+    oracle's float64 scores S (bound 1e-4 * A).  Rows equal to the oracle's
+    ids (selected from fp32(S)) pass outright.  A row that differs must still
+    be a valid choice: ascending distinct causal ids, -1 after them, the right
+    count, every forced decode-window cell present, and no unchosen free cell
+    scoring above a chosen one by more than the two cells' score bounds
+    (which is where fp32 rounding of the scores can swap near-ties)."""
+    got = np.asarray(got)
+    differ = []
+    for t in range(got.shape[0]):
+        if np.array_equal(got[t], ref_ids[t]):
+            continue
+        differ.append(t)
+        p = pos0 + t
+        n = p + 1
+        k = min(n, budget)
+        row = got[t]
+        ids = row[:k]
+        assert np.all(row[k:] == -1), f"{what}: row {t} has ids past its {k} slots"
+        assert np.all(ids >= 0) and np.all(ids <= p) and np.all(np.diff(ids) > 0), \
+            f"{what}: row {t} ids are not ascending distinct causal cells"
+        forced = np.zeros(n, dtype=bool)
+        forced[: min(sink, n)] = True
+        forced[max(sink, p - local): p] = True
+        forced[p] = True
+        chosen = np.zeros(n, dtype=bool)
+        chosen[ids] = True
+        assert np.all(chosen[forced]), f"{what}: row {t} misses a forced cell"
+        pick, left = chosen & ~forced, ~chosen & ~forced
+        if pick.any() and left.any():
+            tol = SCORE_RTOL_A * A[t, :n]
+            lo = np.min(S[t, :n][pick] + tol[pick])
+            hi = np.max(S[t, :n][left] - tol[left])
+            assert lo >= hi, f"{what}: row {t} leaves out a cell that outscores a chosen one beyond the bound"
+    return differ
