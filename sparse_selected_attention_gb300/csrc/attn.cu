@@ -59,6 +59,15 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return r;
 }
 
+// 2^x by the SFU's approximate base-2 exponential (relative error about
+// 2^-22; results below the normal range flush to zero, where a probability
+// is negligible against the running maximum's 1).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
@@ -168,9 +177,12 @@ __device__ __forceinline__ void state_init(State &st) {
 }
 
 // Q fragments of token t for the permuted contraction: slot 2r+e of k-step ks
-// holds d = 32r + 4ks + e, slot 2r+8+e holds d = 32r + 4ks + 2 + e.
+// holds d = 32r + 4ks + e, slot 2r+8+e holds d = 32r + 4ks + 2 + e.  `neg`
+// flips every sign (exact), for a kernel that runs a negative softmax scale
+// as its absolute value.
 template <int S>
-__device__ __forceinline__ void load_q(const AttnLaunch &a, int t, const Geom &geo, uint32_t (&qa)[8][4]) {
+__device__ __forceinline__ void load_q(const AttnLaunch &a, int t, const Geom &geo, uint32_t (&qa)[8][4],
+                                       bool neg = false) {
     const int lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -191,10 +203,11 @@ __device__ __forceinline__ void load_q(const AttnLaunch &a, int t, const Geom &g
 #pragma unroll
             for (int i = 0; i < 16; ++i) w[i] = 0u;
         }
+        const uint32_t flip = neg ? 0x80008000u : 0u;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            qa[ks][half] = w[2 * ks];
-            qa[ks][2 + half] = w[2 * ks + 1];
+            qa[ks][half] = w[2 * ks] ^ flip;
+            qa[ks][2 + half] = w[2 * ks + 1] ^ flip;
         }
     }
 }
@@ -436,29 +449,39 @@ __device__ __forceinline__ void compute_staged(const uint8_t *stp, unsigned vmas
     }
     exchange_s<S>(s, xch, parity);
 
-    float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+    // Online softmax in base 2.  sl2 > 0 (the launch folds a negative scale
+    // into the sign of q), so the maximum of the scaled logits is sl2 times
+    // the maximum of the raw sums, and each probability is one fused
+    // multiply-subtract and one ex2.  Padding cells are masked only in units
+    // that hold some.
+    if (vmask != 0xffffffffu) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const bool v = (vmask >> (8 * j + 2 * r + e)) & 1u;
-            s[j][e] = v ? s[j][e] * sl2 : -CUDART_INF_F;
-            s[j][e + 2] = v ? s[j][e + 2] * sl2 : -CUDART_INF_F;
-            mx0 = fmaxf(mx0, s[j][e]);
-            mx1 = fmaxf(mx1, s[j][e + 2]);
-        }
+            for (int e = 0; e < 2; ++e) {
+                const bool v = (vmask >> (8 * j + 2 * r + e)) & 1u;
+                s[j][e] = v ? s[j][e] : -CUDART_INF_F;
+                s[j][e + 2] = v ? s[j][e + 2] : -CUDART_INF_F;
+            }
+    }
+    float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+    float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+    mx0 = fmaxf(mx0, fmaxf(fmaxf(s[2][0], s[2][1]), fmaxf(s[3][0], s[3][1])));
+    mx1 = fmaxf(mx1, fmaxf(fmaxf(s[2][2], s[2][3]), fmaxf(s[3][2], s[3][3])));
 #pragma unroll
     for (int o = 1; o < 4; o <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
     }
+    mx0 *= sl2;
+    mx1 *= sl2;
     // Lazy rescale: the reference maximum moves only when a unit's maximum
     // exceeds it by more than RESCALE_SLACK (base-2 logits), so the
     // probabilities stay below 2^RESCALE_SLACK and the values are rarely
     // rescaled; the max-first merge only needs a consistent reference.
     const float mn0 = mx0 > st.m[0] + RESCALE_SLACK ? mx0 : st.m[0];
     const float mn1 = mx1 > st.m[1] + RESCALE_SLACK ? mx1 : st.m[1];
-    const float al0 = exp2f(st.m[0] - mn0), al1 = exp2f(st.m[1] - mn1);
+    const float al0 = ex2(st.m[0] - mn0), al1 = ex2(st.m[1] - mn1);
     st.m[0] = mn0;
     st.m[1] = mn1;
     float ps0 = 0.0f, ps1 = 0.0f;
@@ -466,8 +489,8 @@ __device__ __forceinline__ void compute_staged(const uint8_t *stp, unsigned vmas
     for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            s[j][e] = exp2f(s[j][e] - mn0);
-            s[j][e + 2] = exp2f(s[j][e + 2] - mn1);
+            s[j][e] = ex2(fmaf(s[j][e], sl2, -mn0));
+            s[j][e + 2] = ex2(fmaf(s[j][e + 2], sl2, -mn1));
             ps0 += s[j][e];
             ps1 += s[j][e + 2];
         }
@@ -535,14 +558,17 @@ __global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(Att
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
     const int pw = warp / S, half = warp % S;
     const Geom geo = make_geom<S>(a, half);
-    const float sl2 = a.softmax_scale * LOG2E;
+    // |scale| in base 2, floored at the smallest normal float: a zero scale
+    // then still gives exactly uniform weights (every logit rounds to 0) while
+    // a masked -inf stays -inf instead of becoming -inf * 0.
+    const float sl2 = fmaxf(fabsf(a.softmax_scale) * LOG2E, 1.17549435e-38f);
     const int32_t *idrow = a.ids + (size_t)t * a.width;
     const int nunits = a.width / UNIT;
     uint8_t *ring = smem8 + warp * NS * STAGE_BYTES;
     const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
     float *xch = reinterpret_cast<float *>(smem8 + NW * NS * STAGE_BYTES);
     QRegs qsrc;
-    load_q<S>(a, t, geo, qsrc.qa);
+    load_q<S>(a, t, geo, qsrc.qa, a.softmax_scale < 0.0f);
     State st;
     state_init(st);
     bool bad = false;

@@ -152,3 +152,30 @@ def test_other_head_counts(cuda_device, heads):
     q = wl.queries_f16(70, seed=23, heads=heads)
     ids = wl.even_ids(70, 2900, width=1024, select=1000)
     check(q, cache, ids, what=f"{heads} heads")
+
+
+@pytest.mark.parametrize("scale", [-SCALE, 0.0, 0.5, -0.5, 1e-3])
+@pytest.mark.parametrize("part", [False, True])
+def test_softmax_scales(cuda_device, scale, part):
+    """Scales other than 1/sqrt(128): negative (the fused kernel runs |scale|
+    with q's signs flipped), zero (uniform weights), large (logits spread
+    over tens of units, so the running maximum moves often) and tiny."""
+    cache = wl.make_cache(2500, seed=29)
+    q = wl.queries_f16(40, seed=29)
+    ids = wl.even_ids(40, 2400, width=1024, select=1000)
+    ids[3, 100:700] = -1                              # a token with padding inside
+    kq, vq, ksc, vsc = cache_dev(cache)
+    out = torch.full((40, 12, 128), float("nan"), dtype=torch.float16, device="cuda")
+    pt = torch.empty((40, 16, 12, 130), dtype=torch.float32, device="cuda") if part else None
+    qsa_attn(dev(q), kq, vq, ksc, vsc, dev(ids), out, scale, part=pt)
+    torch.cuda.synchronize()
+    ref, _, _, _ = attention(q, cache.kq, cache.vq, cache.ksc, cache.vsc, ids, scale)
+    # At large scales a few cells carry each output, and every p_j * v_j term
+    # keeps the fp16 rounding of p_j and of the dequantised value (together
+    # 2^-10 of |p_j v_j|); the bound adds that to the fp16 tolerance, with
+    # sum_j w_j |v_j| taken from the oracle run on |vq|.
+    mag, _, _, _ = attention(q, cache.kq, np.abs(cache.vq), cache.ksc, cache.vsc, ids, scale)
+    g = out.float().cpu().numpy().astype(np.float64)
+    bound = 2e-3 + 1e-2 * np.abs(ref) + 2.0 ** -10 * mag
+    worst = np.unravel_index(np.argmax(np.abs(g - ref) - bound), g.shape)
+    assert np.all(np.abs(g - ref) <= bound), f"scale {scale}: worst at {worst}: gpu={g[worst]} ref={ref[worst]}"
