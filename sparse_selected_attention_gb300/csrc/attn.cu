@@ -619,17 +619,27 @@ __global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(Att
     __syncthreads();
 
     // Merge: reuse the rings (all copies have landed) for the groups' states.
+    // Value (h, d) of group w sits at (16 w + h) DR + (d ^ 4 (h & 7)): the
+    // XOR spreads one store instruction's 32 rows over all banks (the fewest
+    // wavefronts 512 bytes allow) and keeps the reads of consecutive d
+    // conflict-free.
     constexpr int DR = D * S;  // row length
     float *so = reinterpret_cast<float *>(smem8);
     float *sm = so + NP * 16 * DR;
     float *sl = sm + NP * 16;
     float *ow = so + pw * 16 * DR + D * half;
+    const int sw = 4 * g;
 #pragma unroll
-    for (int jd = 0; jd < 16; ++jd) {
-        ow[g * DR + 32 * r + jd] = st.o[jd][0];
-        ow[g * DR + 32 * r + 16 + jd] = st.o[jd][1];
-        ow[(g + 8) * DR + 32 * r + jd] = st.o[jd][2];
-        ow[(g + 8) * DR + 32 * r + 16 + jd] = st.o[jd][3];
+    for (int jd = 0; jd < 16; jd += 4) {
+        const int d0 = (32 * r + jd) ^ sw, d1 = (32 * r + 16 + jd) ^ sw;
+        *reinterpret_cast<float4 *>(ow + g * DR + d0) =
+            make_float4(st.o[jd][0], st.o[jd + 1][0], st.o[jd + 2][0], st.o[jd + 3][0]);
+        *reinterpret_cast<float4 *>(ow + g * DR + d1) =
+            make_float4(st.o[jd][1], st.o[jd + 1][1], st.o[jd + 2][1], st.o[jd + 3][1]);
+        *reinterpret_cast<float4 *>(ow + (g + 8) * DR + d0) =
+            make_float4(st.o[jd][2], st.o[jd + 1][2], st.o[jd + 2][2], st.o[jd + 3][2]);
+        *reinterpret_cast<float4 *>(ow + (g + 8) * DR + d1) =
+            make_float4(st.o[jd][3], st.o[jd + 1][3], st.o[jd + 2][3], st.o[jd + 3][3]);
     }
     if (r == 0 && half == 0) {
         sm[pw * 16 + g] = st.m[0];
@@ -652,7 +662,7 @@ __global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(Att
                 if (mw == -CUDART_INF_F) continue;
                 const float sc = exp2f(mw - M);
                 L += sc * sl[w * 16 + h];
-                O += sc * so[(w * 16 + h) * DR + d];
+                O += sc * so[(w * 16 + h) * DR + (d ^ (4 * (h & 7)))];
             }
             res = O / L;
         }
