@@ -619,16 +619,18 @@ __global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(Att
     __syncthreads();
 
     // Merge: reuse the rings (all copies have landed) for the groups' states.
-    // Value (h, d) of group w sits at (16 w + h) DR + (d ^ 4 (h & 7)): the
-    // XOR spreads one store instruction's 32 rows over all banks (the fewest
-    // wavefronts 512 bytes allow) and keeps the reads of consecutive d
-    // conflict-free.
+    // Value (h, d) of group w sits at (16 w + h) DR + (d ^ 4 x), x = 2 (d / 32)
+    // + (h & 1).  A 16-byte store is served eight lanes at a time, and the
+    // eight lanes (g, r) with g in {2k, 2k+1} then hit eight different
+    // 16-byte bank groups: four wavefronts per store instruction, the fewest
+    // 512 bytes allow.  The XOR stays inside each 32-float block, so the
+    // reads of consecutive d are conflict-free.
     constexpr int DR = D * S;  // row length
     float *so = reinterpret_cast<float *>(smem8);
     float *sm = so + NP * 16 * DR;
     float *sl = sm + NP * 16;
     float *ow = so + pw * 16 * DR + D * half;
-    const int sw = 4 * g;
+    const int sw = 4 * ((2 * r + (g & 1)) & 7);
 #pragma unroll
     for (int jd = 0; jd < 16; jd += 4) {
         const int d0 = (32 * r + jd) ^ sw, d1 = (32 * r + 16 + jd) ^ sw;
@@ -648,26 +650,43 @@ __global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(Att
         sl[pw * 16 + g + 8] = st.l[1];
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < geo.per * DR; idx += NW * 32) {
-        const int h = idx / DR, d = idx % DR;
+    // Per head: M = max over the groups, and group w's weight 2^(m_w - M) / L
+    // with L = sum_w 2^(m_w - M) l_w (0 for a head with no valid cell, whose
+    // output is then +0), computed once rather than per output element.
+    float *sf = sl + NP * 16;
+    if (threadIdx.x < 16) {
+        const int h = threadIdx.x;
         float M = -CUDART_INF_F;
 #pragma unroll
         for (int w = 0; w < NP; ++w) M = fmaxf(M, sm[w * 16 + h]);
-        float res = 0.0f;
-        if (M != -CUDART_INF_F) {
-            float L = 0.0f, O = 0.0f;
+        float f[NP], L = 0.0f;
 #pragma unroll
-            for (int w = 0; w < NP; ++w) {
-                const float mw = sm[w * 16 + h];
-                if (mw == -CUDART_INF_F) continue;
-                const float sc = exp2f(mw - M);
-                L += sc * sl[w * 16 + h];
-                O += sc * so[(w * 16 + h) * DR + (d ^ (4 * (h & 7)))];
-            }
-            res = O / L;
+        for (int w = 0; w < NP; ++w) {
+            const float mw = sm[w * 16 + h];
+            f[w] = mw == -CUDART_INF_F ? 0.0f : exp2f(mw - M);
+            L += f[w] * sl[w * 16 + h];
+        }
+        const float inv = M == -CUDART_INF_F ? 0.0f : 1.0f / L;
+#pragma unroll
+        for (int w = 0; w < NP; ++w) sf[w * 16 + h] = f[w] * inv;
+    }
+    __syncthreads();
+    // Two adjacent dims per thread: d and d + 1 sit next to each other under
+    // the swizzle (it moves 4-float blocks), and their outputs are one half2.
+    for (int idx = threadIdx.x; idx < geo.per * (DR / 2); idx += NW * 32) {
+        const int h = idx / (DR / 2), d = 2 * (idx % (DR / 2));
+        const int pd = d ^ (4 * ((2 * (d >> 5) + (h & 1)) & 7));
+        float r0 = 0.0f, r1 = 0.0f;
+#pragma unroll
+        for (int w = 0; w < NP; ++w) {
+            const float fw = sf[w * 16 + h];
+            const float2 o = *reinterpret_cast<const float2 *>(so + (w * 16 + h) * DR + pd);
+            r0 = fmaf(fw, o.x, r0);
+            r1 = fmaf(fw, o.y, r1);
         }
         const size_t oi = ((size_t)t * a.n_q_heads + geo.h0 + h) * DR + d;
-        a.out[oi] = __half_as_ushort(__float2half_rn(gated(a, oi, res)));
+        const __half2 hv = __floats2half2_rn(gated(a, oi, r0), gated(a, oi + 1, r1));
+        *reinterpret_cast<__half2 *>(a.out + oi) = hv;
     }
 }
 
@@ -747,7 +766,7 @@ __global__ void __launch_bounds__(D * S) attn_merge_kernel(AttnLaunch a) {
 template <int NW, int NS, int S>
 cudaError_t launch_staged(const AttnLaunch &a, cudaStream_t s) {
     size_t smem = (size_t)NW * NS * STAGE_BYTES + xch_bytes<NW, S>();
-    const size_t merge = (size_t)(NW / S) * (16 * D * S + 32) * sizeof(float);
+    const size_t merge = (size_t)(NW / S) * (16 * D * S + 48) * sizeof(float);
     if (smem < merge) smem = merge;
     cudaError_t e = cudaFuncSetAttribute(attn_staged_kernel<NW, NS, S>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
