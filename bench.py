@@ -65,6 +65,9 @@ def parse():
     p.add_argument("--pages-shape", action="store_true",
                    help="time the attention alone at the pages' own shape (2 KV x 12 heads, head_dim 256, "
                         "per-64 scales) on the same token / id workload")
+    p.add_argument("--decode", action="store_true",
+                   help="latency of the attention alone on the decode windows: 1 token at pos0=320 and the "
+                        "8-token MTP window at pos0=30000 (64 sink + 256 local + own cell, width 384)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-sample-seconds", type=float, default=15.0)
@@ -520,6 +523,53 @@ def run_pages(args, rank, world, local_rank):
     return {"ms": ms, "clocks": clocks, "roofline": roof, "valid_cells": valid}
 
 
+def run_decode(args, rank, world, local_rank):
+    """Per-call device time of qsa_attn on the two decode windows, L2
+    flushed before each call; median over the calls."""
+    import numpy as np
+    import torch
+
+    from sparse_selected_attention_gb300 import qsa_attn
+    from sparse_selected_attention_gb300 import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    res = {}
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    for name, w in (("tiny", wl.TINY_DECODE), ("mtp", wl.MTP_DECODE)):
+        cache = wl.make_cache(w.cells, seed=w.seed + rank)
+
+        def to(x):
+            return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+        kq, vq, ksc, vsc = to(cache.kq), to(cache.vq), to(cache.ksc), to(cache.vsc)
+        q = to(wl.queries_f16(w.ntok, seed=w.seed + rank))
+        ids_np = w.make_ids()
+        ids = to(ids_np)
+        out = torch.empty((w.ntok, HQ, D), dtype=torch.float16, device=dev)
+        for _ in range(args.warmup):
+            qsa_attn(q, kq, vq, ksc, vsc, ids, out)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for k in range(args.steps):
+            flush.zero_()
+            evs[k][0].record(stream)
+            qsa_attn(q, kq, vq, ksc, vsc, ids, out)
+            evs[k][1].record(stream)
+        torch.cuda.synchronize()
+        t = sorted(a.elapsed_time(b) for a, b in evs)
+        ab, valid = attn_bytes(ids_np, w.ntok)
+        res[name] = {"workload": w.name, "us_median": 1e3 * t[len(t) // 2], "us_mean": 1e3 * sum(t) / len(t),
+                     "tokens_per_s": w.ntok / (t[len(t) // 2] / 1e3), "valid_cells": valid,
+                     "algorithmic_bytes": ab}
+    res["clocks"] = sampler.stop()
+    return res
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -559,6 +609,20 @@ def main():
                     "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
                     "data": "synthetic", "config": config, "roofline": res["roofline"], "clocks": res["clocks"],
                     "gpu_launches": args.steps, "valid_cells": res["valid_cells"]}
+            print(json.dumps(line), flush=True)
+        return
+    if args.decode:
+        res = run_decode(args, rank, world, local_rank)
+        if rank == 0:
+            config["workload"] = res["mtp"]["workload"] + "; also " + res["tiny"]["workload"]
+            config.update(ntok=8, pos0=30000, cache_cells=30008, width=384,
+                          l2="flushed before every call (256 MiB write), outside the call's events")
+            line = {"metric": "decode attention latency (device time per qsa_attn call)",
+                    "value": res["mtp"]["us_median"], "unit": "us", "n_gpus": world, "steps": args.steps,
+                    "warmup": args.warmup, "ms_per_step": res["mtp"]["us_median"] / 1e3,
+                    "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+                    "data": "synthetic", "config": config, "decode": {k: res[k] for k in ("mtp", "tiny")},
+                    "clocks": res["clocks"], "gpu_launches": 2 * args.steps}
             print(json.dumps(line), flush=True)
         return
     res = run_ours(args, rank, world, local_rank)
