@@ -68,6 +68,9 @@ def parse():
     p.add_argument("--decode", action="store_true",
                    help="latency of the attention alone on the decode windows: 1 token at pos0=320 and the "
                         "8-token MTP window at pos0=30000 (64 sink + 256 local + own cell, width 384)")
+    p.add_argument("--score-sweep", action="store_true",
+                   help="the score pass alone from fp32 queries (head-sum pass + tcgen05 score) at T=1984 and "
+                        "pos0 = 0, 2048, 8192, 30000")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-sample-seconds", type=float, default=15.0)
@@ -570,6 +573,59 @@ def run_decode(args, rank, world, local_rank):
     return res
 
 
+def run_score_sweep(args, rank, world, local_rank):
+    """qsa_score from fp32 queries N(0,1) [T, 12, 128] (its own head-sum pass
+    plus the score kernel) at each pos0 of the sweep; L2 flushed before each
+    call; mean device time per call."""
+    import numpy as np
+    import torch
+
+    from sparse_selected_attention_gb300 import qsa_score, qsa_score_workspace_bytes
+    from sparse_selected_attention_gb300 import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    peak, peak_src = peaks()
+    T = args.ntok
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    out = []
+    for pos0 in wl.SCORE_POS0:
+        C = pos0 + T
+        cache = wl.make_cache(C, seed=5 + rank)
+
+        def to(x):
+            return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+        kq, ksc = to(cache.kq), to(cache.ksc)
+        q = to(wl.queries_f32(T, seed=5 + rank))
+        scores = torch.empty((T, C), dtype=torch.float32, device=dev)
+        ws = torch.empty(qsa_score_workspace_bytes(T), dtype=torch.uint8, device=dev)
+        for _ in range(args.warmup):
+            qsa_score(q, kq, ksc, pos0, scores, ws)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for k in range(args.steps):
+            flush.zero_()
+            evs[k][0].record(stream)
+            qsa_score(q, kq, ksc, pos0, scores, ws)
+            evs[k][1].record(stream)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+        pairs = score_pairs(T, pos0)
+        # bytes: fp32 queries read by the head-sum pass and its fp16 hi/lo rows,
+        # then the score kernel's bytes
+        nb = T * HQ * D * 4 + 2 * (-(-T // 64) * 64) * 2 * D * 2 + score_bytes(T, pos0, C)
+        out.append({"pos0": pos0, "cells": C, "pairs": pairs, "us": 1e3 * ms,
+                    "gbs": nb / (ms / 1e3) / 1e9, "frac_hbm": nb / (ms / 1e3) / 1e9 / peak,
+                    "tflops_algorithmic_12_heads": 2 * HQ * D * pairs / (ms / 1e3) / 1e12,
+                    "tflops_executed_head_sum_hi_lo": 2 * 2 * D * pairs / (ms / 1e3) / 1e12})
+    return {"sweep": out, "clocks": sampler.stop(), "peak": peak, "peak_source": peak_src}
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -609,6 +665,24 @@ def main():
                     "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
                     "data": "synthetic", "config": config, "roofline": res["roofline"], "clocks": res["clocks"],
                     "gpu_launches": args.steps, "valid_cells": res["valid_cells"]}
+            print(json.dumps(line), flush=True)
+        return
+    if args.score_sweep:
+        res = run_score_sweep(args, rank, world, local_rank)
+        if rank == 0:
+            last = res["sweep"][-1]
+            config["workload"] = ("score pass sweep: fp32 queries N(0,1) [%d, 12, 128] against the int8 key cache, "
+                                  "pos0 in (0, 2048, 8192, 30000), every causal cell" % args.ntok)
+            config["l2"] = "flushed before every call (256 MiB write), outside the call's events"
+            line = {"metric": "score pass throughput (query tokens/s) at pos0=30000; the sweep in 'sweep'",
+                    "value": args.ntok / (last["us"] / 1e6), "unit": "tokens/s", "n_gpus": world,
+                    "steps": args.steps, "warmup": args.warmup, "ms_per_step": last["us"] / 1e3,
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+                    "data": "synthetic", "config": config, "sweep": res["sweep"],
+                    "roofline": {"bound": "hbm", "achieved": last["gbs"], "peak": res["peak"], "unit": "GB/s",
+                                 "frac": last["frac_hbm"], "traffic": None, "kernel": "score (pos0=30000)",
+                                 "peak_source": res["peak_source"]},
+                    "clocks": res["clocks"], "gpu_launches": 2 * args.steps * len(res["sweep"])}
             print(json.dumps(line), flush=True)
         return
     if args.decode:

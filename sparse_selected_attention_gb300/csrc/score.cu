@@ -87,14 +87,25 @@ constexpr uint32_t IDESC = idesc_f16(TM, TN, false, false);
 template <bool F16>
 __global__ void __launch_bounds__(D) qsum_kernel(ScoreLaunch a) {
     const int t = blockIdx.x, d = threadIdx.x;
+    // Heads added in order from +0 (the order qsa_prep's head sum uses too);
+    // the loads are issued sixteen heads at a time so that a token's rows
+    // cost one memory round trip per sixteen heads, not one per head.
+    constexpr int HB = 16;
     float s = 0.0f;
     if (t < a.ntok) {
-        if (F16) {
-            const __half *q = reinterpret_cast<const __half *>(a.q) + (size_t)t * a.n_q_heads * D + d;
-            for (int h = 0; h < a.n_q_heads; ++h) s += __half2float(q[(size_t)h * D]);
-        } else {
-            const float *q = reinterpret_cast<const float *>(a.q) + (size_t)t * a.n_q_heads * D + d;
-            for (int h = 0; h < a.n_q_heads; ++h) s += __ldg(q + (size_t)h * D);
+        for (int h0 = 0; h0 < a.n_q_heads; h0 += HB) {
+            float v[HB];
+#pragma unroll
+            for (int i = 0; i < HB; ++i) {
+                const int h = h0 + i;
+                const size_t off = ((size_t)t * a.n_q_heads + h) * D + d;
+                v[i] = h >= a.n_q_heads ? 0.0f
+                       : F16          ? __half2float(__ldg(reinterpret_cast<const __half *>(a.q) + off))
+                                      : __ldg(reinterpret_cast<const float *>(a.q) + off);
+            }
+#pragma unroll
+            for (int i = 0; i < HB; ++i)
+                if (h0 + i < a.n_q_heads) s += v[i];
         }
     }
     const __half hi = __float2half_rn(s);
