@@ -139,6 +139,13 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
 }
 
+// Eight consecutive 32-bit columns of tensor memory for the warp's 32 lanes.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr));
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, uint32_t src) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
@@ -325,6 +332,9 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
         // Fully causal tiles are combined into a token-major fp32 tile in
         // shared memory and written by one TMA bulk-tensor store; tiles that
         // cross the causal boundary are stored element-wise under the mask.
+        // A warp drains its 32 cells x 32 tokens in four 8-token pieces, the
+        // tensor-memory loads of each piece issued before the previous piece
+        // is combined and stored, so their latency hides behind that work.
         Walker w = w0;
         int nfull = 0;
         for (int k = 0; k < n; ++k) {
@@ -343,24 +353,27 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
             const float ks3 = __half2float(__ushort_as_half((unsigned short)(kv.y >> 16)));
             const uint64_t k0 = pack2(ks0, ks0), k1 = pack2(ks1, ks1), k2 = pack2(ks2, ks2), k3 = pack2(ks3, ks3);
             const uint32_t cbuf = sC + (nfull & 1) * C_BYTES;
-            if (full) {
-                // The store issued two full tiles ago read this buffer.
-                if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                named_sync_epilogue();
-            }
             const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NG * TN + half * (TN / 2));
             const int tmin = cell - a.pos0;  // first token whose causal range reaches `cell`
-#pragma unroll 1
-            for (int j0 = 0; j0 < TN / 2; j0 += 16) {
-                const int tj = t0 + half * (TN / 2) + j0;  // first token of this 16-column chunk
-                if (!full && tj >= a.ntok) break;  // warp-uniform
-                uint32_t v[NG][16];
+            const int tw = t0 + half * (TN / 2);  // first token of this warp's 32 columns
+            uint32_t va[NG][8], vb[NG][8];
+            auto load8 = [&](uint32_t (&v)[NG][8], int j0) {
 #pragma unroll
-                for (int g = 0; g < NG; ++g) tmem_ld16(tbase + g * TN + j0, v[g]);
+                for (int g = 0; g < NG; ++g) tmem_ld8(tbase + g * TN + j0, v[g]);
+            };
+            // After the wait: each loaded register passes through an empty
+            // volatile statement, so no use of it can move above the wait.
+            auto wait8 = [&](uint32_t (&v)[NG][8]) {
                 tmem_wait_ld();
-                float o[16];
 #pragma unroll
-                for (int j = 0; j < 16; j += 2) {
+                for (int g = 0; g < NG; ++g)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) asm volatile("" : "+r"(v[g][j]));
+            };
+            auto drain8 = [&](const uint32_t (&v)[NG][8], int j0) {
+                float o[8];
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {
                     uint64_t acc = fma2(k0, pack2(__uint_as_float(v[0][j]), __uint_as_float(v[0][j + 1])), 0ull);
                     acc = fma2(k1, pack2(__uint_as_float(v[1][j]), __uint_as_float(v[1][j + 1])), acc);
                     acc = fma2(k2, pack2(__uint_as_float(v[2][j]), __uint_as_float(v[2][j + 1])), acc);
@@ -368,24 +381,41 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a, const 
                     o[j] = __uint_as_float((uint32_t)acc);
                     o[j + 1] = __uint_as_float((uint32_t)(acc >> 32));
                 }
+                const int tj = tw + j0;
                 if (full) {
                     const uint32_t dst = cbuf + (uint32_t)((tj - t0) * TM + quarter * 32 + lane) * 4;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
+                    for (int j = 0; j < 8; ++j)
                         asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + j * TM * 4), "f"(o[j]) : "memory");
                 } else {
                     float *dst = a.scores + (size_t)tj * a.ld + cell;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
+                    for (int j = 0; j < 8; ++j) {
                         const int t = tj + j;
                         if (t < a.ntok && t >= tmin) dst[(size_t)j * a.ld] = o[j];
                     }
                 }
-            }
+            };
+            load8(va, 0);
+            wait8(va);
+            load8(vb, 8);
+            drain8(va, 0);
+            wait8(vb);
+            load8(va, 16);
+            drain8(vb, 8);
+            wait8(va);
+            load8(vb, 24);
+            drain8(va, 16);
+            wait8(vb);
+            drain8(vb, 24);
             fence_before();
             mbar_arrive(acc_empty + 8 * b);
             if (full) {
                 fence_async_smem();
+                // The store issued at the previous full tile reads the other
+                // buffer, which the next full tile writes: its read must be
+                // over before the barrier that lets the writers go on.
+                if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                 named_sync_epilogue();
                 if (tid == 0) tma_store_2d(&tmap, c0, t0, cbuf);
                 ++nfull;
