@@ -1,0 +1,60 @@
+"""The algorithmic bytes and pairs behind bench.py's roofline figures, against
+closed forms worked out by hand from the workload definitions (no GPU).
+
+Attention moves 272 B per valid selected cell (128 + 128 int8 code bytes and
+2 x 4 fp16 group scales), 4 B per id slot, and the fp16 q and output rows.
+The score writes one fp32 value per causal (token, cell) pair.  Selection
+reads every free causal score once and writes W ids per token.
+"""
+import numpy as np
+import pytest
+
+import bench
+from sparse_selected_attention_gb300 import workloads as wl
+
+T, W = 1984, 2048
+QOUT = 2 * T * 12 * 128 * 2  # fp16 q in and fp16 out
+
+
+def test_long_context_attention_bytes():
+    ids = wl.even_ids(T, 30000, W)
+    nbytes, valid = bench.attn_bytes(ids, T)
+    assert valid == T * W                       # every token selects 2048 of its 30001+ cells
+    assert nbytes == T * W * 272 + T * W * 4 + QOUT == 1_133_641_728
+
+
+def test_short_context_attention_bytes():
+    ids = wl.even_ids(T, 0, W)
+    nbytes, valid = bench.attn_bytes(ids, T)
+    assert valid == T * (T + 1) // 2 == 1_969_120  # token t sees cells 0..t
+    assert nbytes == valid * 272 + T * W * 4 + QOUT
+
+
+@pytest.mark.parametrize("pos0", [0, 2048, 8192, 30000])
+def test_score_pairs(pos0):
+    # token t (position pos0 + t) scores cells 0 .. pos0 + t
+    assert bench.score_pairs(T, pos0) == sum(pos0 + t + 1 for t in range(T)) == T * pos0 + 1_969_120
+
+
+def test_selection_bytes():
+    # p = pos0 + t >= 320: the free range is [64, p - 256), p - 320 cells
+    free = sum(p - 320 for p in range(30000, 30000 + T))
+    assert free == 60_852_256
+    assert bench.select_bytes(T, 30000) == 4 * free + 4 * T * W == 259_661_952
+    # short rows: no free cells below p = 320
+    assert bench.select_bytes(1, 100) == 4 * W
+
+
+def test_pages_shape_attention_bytes():
+    ids = wl.even_ids(T, 30000, W)
+    nbytes, valid = bench.attn_bytes(ids, T, hkv=2, hq=24, d=256)
+    per_cell = 2 * (2 * 256 + 2 * 4 * 2)        # two KV heads x (K and V codes + 4 scales each)
+    assert per_cell == 1056
+    assert nbytes == valid * per_cell + T * W * 4 + 2 * T * 24 * 256 * 2
+
+
+def test_prep_bytes_per_token():
+    per = 12 * 128 * (4 + 2) + 2 * 128 * 4 + 2 * (128 + 2 * 4)   # q in/out, k and v in, codes + scales out
+    pad = -(-T // 64) * 64
+    assert bench.prep_bytes(T) == T * per + pad * 2 * 128 * 2 + 128 * 4
+    assert bench.prep_bytes(T) == pytest.approx(21.87e6, rel=1e-3)
