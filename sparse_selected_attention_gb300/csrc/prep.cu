@@ -6,10 +6,10 @@
 // scales by rs and the weight g, and rotates dims below QROT with partner
 // tid ^ 32.
 //
-// One CTA per token.  Warps 0..Hq-1 own the query rows of that token, warp Hq
-// the K row and warp Hq+1 the V row.  With head_dim 128 every lane holds four
-// consecutive elements, so a row is one coalesced 512-byte load and a sum of
-// squares is five xor-shuffles.  The token's rotation angles are computed once
+// One CTA per token.  Each of the first ceil(Hq/3) warps owns three of the
+// token's query rows, the next warp the K row and the last the V row.  With
+// head_dim 128 every lane holds four consecutive elements, so a row is one
+// coalesced 512-byte load and a sum of squares is five xor-shuffles.  The token's rotation angles are computed once
 // per CTA (the product p * inv_freq exactly in double, reduced modulo 2*pi,
 // then an fp32 sincos) because a single fp32 product p * inv_freq is off by up
 // to 2e-3 rad at p ~ 32k.  The frequency table itself is computed once per
@@ -38,7 +38,15 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 constexpr int MAXQH = 30;  // query heads per token (the launcher's limit)
 
-__global__ void __launch_bounds__(1024) prep_kernel(PrepParams P) {
+// HPW query heads per warp: warps 0 .. ceil(Hq/HPW)-1 own the query rows,
+// the next two the K and the V row.  Three heads per warp keeps a token's
+// CTA at 6 warps for 12 heads (at most 384 threads for the launcher's 30),
+// so eight tokens' CTAs fit on an SM at 40 registers; prep is bound by each
+// token's latency chain, and more tokens in flight hide it.  (One head per
+// warp, 14 warps per token: 14.4 us at the 1984-token workload; three: 12.9.)
+constexpr int HPW = 3;
+
+__global__ void __launch_bounds__(384, 4) prep_kernel(PrepParams P) {
     const PrepLaunch &a = P.a;
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -52,16 +60,24 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepParams P) {
     const int half = a.rope_dims >> 1;
 
     // Issue this warp's row loads before the angle table is built.
-    const bool is_q = warp < a.n_q_heads, is_kv = !is_q && warp < a.n_q_heads + 2;
-    const bool is_v = warp == a.n_q_heads + 1;
-    const size_t row = ((size_t)t * a.n_q_heads + warp) * D;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), g = x;
+    const int nqw = (a.n_q_heads + HPW - 1) / HPW;
+    const bool is_q = warp < nqw, is_kv = !is_q && warp < nqw + 2;
+    const bool is_v = warp == nqw + 1;
+    float4 xs[HPW], g = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < HPW; ++j) xs[j] = g;
     if (is_q) {
-        x = __ldg(reinterpret_cast<const float4 *>(a.q_in + row) + lane);
         g = __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane);
+#pragma unroll
+        for (int j = 0; j < HPW; ++j) {
+            const int h = HPW * warp + j;
+            if (h < a.n_q_heads)
+                xs[j] = __ldg(reinterpret_cast<const float4 *>(a.q_in + ((size_t)t * a.n_q_heads + h) * D) + lane);
+        }
     } else if (is_kv) {
-        x = __ldg(reinterpret_cast<const float4 *>((is_v ? a.v_in : a.k_in) + (size_t)t * D) + lane);
+        xs[0] = __ldg(reinterpret_cast<const float4 *>((is_v ? a.v_in : a.k_in) + (size_t)t * D) + lane);
     }
+    const float4 x = xs[0];
 
     if ((int)threadIdx.x < half) {
         const int i = threadIdx.x;
@@ -81,41 +97,60 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepParams P) {
     __syncthreads();
 
     if (is_q) {
-        float ss = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
-        ss = warp_sum(ss);
-        const float rs = __frsqrt_rn(ss / (float)D + a.eps);
-        float y[4] = {(rs * x.x) * g.x, (rs * x.y) * g.y, (rs * x.z) * g.z, (rs * x.w) * g.w};
+        // The warp's rows side by side: their shuffle chains interleave.
+        float y[HPW][4];
+#pragma unroll
+        for (int j = 0; j < HPW; ++j) {
+            const float4 xj = xs[j];
+            float ss = xj.x * xj.x + xj.y * xj.y + xj.z * xj.z + xj.w * xj.w;
+            ss = warp_sum(ss);
+            const float rs = __frsqrt_rn(ss / (float)D + a.eps);
+            y[j][0] = (rs * xj.x) * g.x;
+            y[j][1] = (rs * xj.y) * g.y;
+            y[j][2] = (rs * xj.z) * g.z;
+            y[j][3] = (rs * xj.w) * g.w;
+        }
         if (half > 0) {
             const int sh = half >> 2;  // lanes between partners (half is a multiple of 4)
-            float up[4], dn[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                up[e] = __shfl_down_sync(0xffffffffu, y[e], sh);
-                dn[e] = __shfl_up_sync(0xffffffffu, y[e], sh);
-            }
             const int i0 = lane * 4;
-            if (i0 < half) {
+#pragma unroll
+            for (int j = 0; j < HPW; ++j) {
+                float up[4], dn[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float2 c = cs[i0 + e];
-                    y[e] = y[e] * c.x - up[e] * c.y;
+                    up[e] = __shfl_down_sync(0xffffffffu, y[j][e], sh);
+                    dn[e] = __shfl_up_sync(0xffffffffu, y[j][e], sh);
                 }
-            } else if (i0 < 2 * half) {
+                if (i0 < half) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 c = cs[i0 - half + e];
-                    y[e] = y[e] * c.x + dn[e] * c.y;
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 c = cs[i0 + e];
+                        y[j][e] = y[j][e] * c.x - up[e] * c.y;
+                    }
+                } else if (i0 < 2 * half) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 c = cs[i0 - half + e];
+                        y[j][e] = y[j][e] * c.x + dn[e] * c.y;
+                    }
                 }
             }
         }
-        if (a.qbar) qrows[warp][lane] = make_float4(y[0], y[1], y[2], y[3]);
-        const __half2 h01 = __floats2half2_rn(y[0], y[1]);
-        const __half2 h23 = __floats2half2_rn(y[2], y[3]);
-        uint2 hv;
-        hv.x = *reinterpret_cast<const uint32_t *>(&h01);
-        hv.y = *reinterpret_cast<const uint32_t *>(&h23);
-        reinterpret_cast<uint2 *>(a.q_out + row)[lane] = hv;
-        if (a.q_out_f32) reinterpret_cast<float4 *>(a.q_out_f32 + row)[lane] = make_float4(y[0], y[1], y[2], y[3]);
+#pragma unroll
+        for (int j = 0; j < HPW; ++j) {
+            const int h = HPW * warp + j;
+            if (h >= a.n_q_heads) continue;
+            const size_t row = ((size_t)t * a.n_q_heads + h) * D;
+            if (a.qbar) qrows[h][lane] = make_float4(y[j][0], y[j][1], y[j][2], y[j][3]);
+            const __half2 h01 = __floats2half2_rn(y[j][0], y[j][1]);
+            const __half2 h23 = __floats2half2_rn(y[j][2], y[j][3]);
+            uint2 hv;
+            hv.x = *reinterpret_cast<const uint32_t *>(&h01);
+            hv.y = *reinterpret_cast<const uint32_t *>(&h23);
+            reinterpret_cast<uint2 *>(a.q_out + row)[lane] = hv;
+            if (a.q_out_f32)
+                reinterpret_cast<float4 *>(a.q_out_f32 + row)[lane] = make_float4(y[j][0], y[j][1], y[j][2], y[j][3]);
+        }
     } else if (is_kv) {
         int8_t *dst = (is_v ? a.vq : a.kq) + (size_t)(a.pos0 + t) * D;
         uint16_t *sdst = (is_v ? a.vsc : a.ksc) + (size_t)(a.pos0 + t) * (D / G);
@@ -184,7 +219,7 @@ cudaError_t launch_prep(const PrepLaunch &a, cudaStream_t s) {
     PrepParams P{a};
     for (int i = 0; i < a.rope_dims / 2; ++i)
         P.a.inv_freq[i] = (float)std::pow((double)a.rope_theta, -2.0 * (double)i / (double)a.rope_dims);
-    const int threads = 32 * (a.n_q_heads + 2);
+    const int threads = 32 * ((a.n_q_heads + HPW - 1) / HPW + 2);  // <= 384 for n_q_heads <= 30
     prep_kernel<<<a.qbar ? a.ntok_pad : a.ntok, threads, 0, s>>>(P);
     return cudaGetLastError();
 }
