@@ -47,6 +47,13 @@ def test_prep_shapes(cuda_device, T, pos0):
     run_case(T, pos0)
 
 
+@pytest.mark.parametrize("heads", [1, 2, 4, 5, 7, 8, 16, 29, 30])
+def test_prep_head_counts(cuda_device, heads):
+    """Query rows are dealt three to a warp: head counts that leave the last
+    query warp one or two rows short, and the launcher's maximum of 30."""
+    run_case(37, 900, heads=heads, seed=50 + heads)
+
+
 @pytest.mark.parametrize("rope_dims", [0, 8, 128])
 def test_prep_rope_dims(cuda_device, rope_dims):
     run_case(19, 1234, rope_dims=rope_dims)
