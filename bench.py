@@ -39,6 +39,7 @@ sys.path.insert(0, ROOT)
 METRIC = "query tokens/s and achieved HBM GB/s (% of roofline) for QSA attention at T=1984"
 UNIT = "tokens/s"
 NTOK, POS0, WIDTH, HQ, D, G = 1984, 30000, 2048, 12, 128, 32
+SCORE_CTAS = 0  # 0: the overlapped score fills the attention's tail (a fixed SM share measured slower)
 WORKLOAD = ("prompt attention long context: T=1984 query tokens, pos0=30000, int8 K/V cache of 31984 cells "
             "with fp16 per-32 scales, 12 q heads / 1 KV head, head_dim 128, 2048 evenly spaced causal ids per "
             "token; step = qsa_prep + qsa_score (all causal cells, from the head sum of the fp32 rotated queries that "
@@ -71,6 +72,8 @@ def parse():
     p.add_argument("--score-sweep", action="store_true",
                    help="the score pass alone from fp32 queries (head-sum pass + tcgen05 score) at T=1984 and "
                         "pos0 = 0, 2048, 8192, 30000")
+    p.add_argument("--score-ctas", type=int, default=SCORE_CTAS,
+                   help="SMs the overlapped score takes (0: it fills the attention's tail instead)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-sample-seconds", type=float, default=15.0)
@@ -305,11 +308,17 @@ def run_ours(args, rank, world, local_rank):
     names = KERNELS_SELECT if args.select else KERNELS
 
     main_bufs = {"q": q_in, "k": k_in, "v": v_in, "ids": ids, "out": out}
-    # Score and attention both depend only on prep, so without selection the
-    # score runs on a second stream beside the attention (it is bound by DRAM
-    # writes, the attention by instruction issue on an L2-resident cache);
-    # the step ends when both have.  With selection the chain is serial.
-    side = torch.cuda.Stream(dev)
+    # Score and attention both depend only on prep, so without selection they
+    # run side by side and the step ends when both have; with selection the
+    # chain is serial.  Neither kernel's CTAs fit on an SM beside the other's,
+    # so they split the SMs: the score, on a high-priority stream and launched
+    # first, takes `score_ctas` SMs (its persistent CTAs are placed before any
+    # attention CTA), and the attention's CTAs fill the others.  A score CTA
+    # turns out more scores per SM-second on a share of the GPU than on all of
+    # it, where the SMs contend for DRAM writes.  With score_ctas = 0 the
+    # attention goes first and the score's full grid fills its tail.
+    sc = args.score_ctas
+    side = torch.cuda.Stream(dev, priority=-1) if sc > 0 else torch.cuda.Stream(dev)
     ev_prep, ev_side = torch.cuda.Event(), torch.cuda.Event()
 
     def timed(ev, name, st, fn):
@@ -333,9 +342,13 @@ def run_ours(args, rank, world, local_rank):
         else:
             ev_prep.record(stream)
             side.wait_event(ev_prep)
+            run_score = lambda: timed(ev, "score", side, lambda: qsa_score(
+                None, kq, ksc, pos0, scores, ws, stream=side, workspace_holds_qbar=True, max_ctas=sc))
+            if sc > 0:
+                run_score()
             timed(ev, "attn", stream, lambda: qsa_attn(q16, kq, vq, ksc, vsc, b["ids"], b["out"]))
-            timed(ev, "score", side,
-                  lambda: qsa_score(None, kq, ksc, pos0, scores, ws, stream=side, workspace_holds_qbar=True))
+            if sc == 0:
+                run_score()
             ev_side.record(side)
             stream.wait_event(ev_side)
         if ev:

@@ -35,7 +35,7 @@
 extern "C" {
 #endif
 
-#define QSA_ABI_VERSION 2
+#define QSA_ABI_VERSION 3
 
 typedef enum {
     QSA_OK = 0,
@@ -120,6 +120,10 @@ typedef struct {
  * already filled it through qsa_prep's qbar_out for the same tokens, q is
  * ignored (it may be NULL) and the head-sum pass is skipped; the scores are
  * bit-identical to those computed from the fp32 q_out_f32 of that prep.
+ * max_ctas: 0 runs one persistent CTA per SM (each CTA takes a whole SM's
+ * shared memory); n > 0 runs at most n.  A caller that overlaps the score with
+ * other kernels on another stream caps it so that those kernels keep the
+ * remaining SMs; the scores do not depend on the cap.  Negative is rejected.
  * Requires pos0 + ntok <= cache_cells.  Supported: head_dim == 128,
  * group == 32, 1 <= n_q_heads <= 64.  q, kq 16-byte aligned; ksc 8-byte.
  */
@@ -135,6 +139,7 @@ typedef struct {
     size_t workspace_bytes;
     unsigned int *err;
     int workspace_holds_qbar; /* added in ABI version 2: 0 or 1, see above */
+    int max_ctas;             /* added in ABI version 3: 0 = one CTA per SM, n > 0 = at most n, see above */
 } qsa_score_args;
 
 /* Bytes of workspace qsa_score needs for `ntok` tokens (0 on bad input). */
@@ -200,7 +205,7 @@ typedef struct {
  * (QSA_SCORE_NOALLOC_MAX_TOKENS * 512 bytes = 4 MiB of device memory, held on
  * every GPU that loads the library until the process exits).  The
  * `workspace`, `workspace_bytes` and `workspace_holds_qbar` fields are ignored:
- * the head sum is always computed from q.
+ * the head sum is always computed from q; `max_ctas` applies as in qsa_score.
  *
  *  - ntok above QSA_SCORE_NOALLOC_MAX_TOKENS is rejected with
  *    QSA_ERR_INVALID_ARG; nothing is enqueued.

@@ -77,12 +77,14 @@ def qsa_prep(q_in, k_in, v_in, norm_w, pos0, kq, vq, ksc, vsc, q_out, q_out_f32=
 
 
 def qsa_score(q, kq, ksc, pos0, scores, workspace, err=None, stream=None, workspace_holds_qbar=False,
-              n_q_heads=12):
+              n_q_heads=12, max_ctas=0):
     """scores[t, c] for c <= pos0 + t (others untouched).  q [T, Hq, D] fp32 or
     fp16; scores [T, ld] fp32 with ld >= pos0 + T; workspace a uint8 CUDA
     tensor of at least qsa_score_workspace_bytes(T) bytes.  With
     workspace_holds_qbar=True the workspace was filled by qsa_prep(qbar_out=)
-    for these tokens and q may be None (T is then scores.shape[0])."""
+    for these tokens and q may be None (T is then scores.shape[0]).
+    max_ctas > 0 caps the persistent CTAs (one per SM when 0), leaving the
+    other SMs to kernels on other streams."""
     import torch
     if q is None:
         if not workspace_holds_qbar:
@@ -102,11 +104,11 @@ def qsa_score(q, kq, ksc, pos0, scores, workspace, err=None, stream=None, worksp
                        scores=_ptr(scores, "scores", torch.float32), ld=scores.shape[1],
                        workspace=_ptr(workspace, "workspace"),
                        workspace_bytes=workspace.numel() * workspace.element_size(),
-                       err=_ptr(err, "err", torch.int32, optional=True))
+                       err=_ptr(err, "err", torch.int32, optional=True), max_ctas=int(max_ctas))
     _abi.check(lib().qsa_score(ctypes.byref(a), _stream(stream)))
 
 
-def qsa_score_noalloc(q, kq, ksc, pos0, scores, err=None, stream=None):
+def qsa_score_noalloc(q, kq, ksc, pos0, scores, err=None, stream=None, max_ctas=0):
     """qsa_score without a caller workspace, for callers that cannot allocate
     device memory when they score.  It uses the library's built-in scratch
     (at most 8192 tokens), so calls must not overlap on the GPU."""
@@ -120,7 +122,8 @@ def qsa_score_noalloc(q, kq, ksc, pos0, scores, err=None, stream=None):
                        q=_ptr(q, "q"), q_dtype=_abi.QSA_F16 if q.dtype == torch.float16 else _abi.QSA_F32,
                        kq=_ptr(kq, "kq", torch.int8), ksc=_ptr(ksc, "ksc", torch.float16),
                        scores=_ptr(scores, "scores", torch.float32), ld=scores.shape[1],
-                       workspace=None, workspace_bytes=0, err=_ptr(err, "err", torch.int32, optional=True))
+                       workspace=None, workspace_bytes=0, err=_ptr(err, "err", torch.int32, optional=True),
+                       max_ctas=int(max_ctas))
     _abi.check(lib().qsa_score_noalloc(ctypes.byref(a), _stream(stream)))
 
 

@@ -36,7 +36,7 @@ class ScoreArgs(ctypes.Structure):
                 ("group", _c_int), ("cache_cells", _c_int),
                 ("q", _vp), ("q_dtype", _c_int), ("kq", _vp), ("ksc", _vp), ("scores", _vp),
                 ("ld", ctypes.c_int64), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("err", _vp),
-                ("workspace_holds_qbar", _c_int)]
+                ("workspace_holds_qbar", _c_int), ("max_ctas", _c_int)]
 
 
 class SelectArgs(ctypes.Structure):
@@ -57,7 +57,7 @@ class QSAError(RuntimeError):
         self.status = status
 
 
-ABI_VERSION = 2  # the struct layouts above
+ABI_VERSION = 3  # the struct layouts above
 _lib = None
 
 

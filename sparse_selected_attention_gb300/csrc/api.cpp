@@ -113,6 +113,7 @@ qsa_status qsa_score(const qsa_score_args *a, void *stream) {
     if (a->ld < (long long)a->pos0 + a->ntok) return fail(QSA_ERR_INVALID_ARG, "qsa_score: ld < pos0 + ntok");
     if (a->workspace_holds_qbar != 0 && a->workspace_holds_qbar != 1)
         return fail(QSA_ERR_INVALID_ARG, "qsa_score: workspace_holds_qbar must be 0 or 1");
+    if (a->max_ctas < 0) return fail(QSA_ERR_INVALID_ARG, "qsa_score: negative max_ctas");
     if (a->ntok == 0) return QSA_OK;
     const bool need_q = !a->workspace_holds_qbar;
     if ((need_q && !a->q) || !a->kq || !a->ksc || !a->scores || !a->workspace)
@@ -124,7 +125,7 @@ qsa_status qsa_score(const qsa_score_args *a, void *stream) {
         return fail(QSA_ERR_INVALID_ARG, "qsa_score: misaligned buffer");
     qsa::ScoreLaunch L{a->ntok,   a->pos0, a->n_q_heads, a->cache_cells, a->q, a->q_dtype == QSA_F16 ? 1 : 0,
                        a->kq,     a->ksc,  a->scores,    a->ld,          static_cast<uint16_t *>(a->workspace),
-                       a->err,    a->workspace_holds_qbar};
+                       a->err,    a->workspace_holds_qbar, a->max_ctas};
     cudaError_t e = qsa::launch_score(L, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_score");
 }
@@ -194,12 +195,14 @@ qsa_status qsa_score_noalloc(const qsa_score_args *a, void *stream) {
     if ((long long)a->pos0 + a->ntok > a->cache_cells)
         return fail(QSA_ERR_INVALID_ARG, "qsa_score_noalloc: pos0 + ntok exceeds cache_cells");
     if (a->ld < (long long)a->pos0 + a->ntok) return fail(QSA_ERR_INVALID_ARG, "qsa_score_noalloc: ld < pos0 + ntok");
+    if (a->max_ctas < 0) return fail(QSA_ERR_INVALID_ARG, "qsa_score_noalloc: negative max_ctas");
     if (a->ntok == 0) return QSA_OK;
     if (!a->q || !a->kq || !a->ksc || !a->scores) return fail(QSA_ERR_INVALID_ARG, "qsa_score_noalloc: NULL buffer");
     if (!aligned(a->q, 16) || !aligned(a->kq, 16) || !aligned(a->ksc, 8) || !aligned(a->scores, 4))
         return fail(QSA_ERR_INVALID_ARG, "qsa_score_noalloc: misaligned buffer");
     qsa::ScoreLaunch L{a->ntok, a->pos0, a->n_q_heads, a->cache_cells, a->q, a->q_dtype == QSA_F16 ? 1 : 0,
-                       a->kq,   a->ksc,  a->scores,    a->ld,          nullptr, a->err};
+                       a->kq,   a->ksc,  a->scores,    a->ld,          nullptr, a->err,
+                       0,       a->max_ctas};
     cudaError_t e = qsa::launch_score_noalloc(L, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_score_noalloc");
 }

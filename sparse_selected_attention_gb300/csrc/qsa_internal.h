@@ -33,6 +33,7 @@ struct ScoreLaunch {
     uint16_t *qsum;  // workspace: [ntok_pad, 2, 128] fp16 (hi row, lo row)
     unsigned int *err;
     int qsum_ready;  // the workspace already holds the head sum (written by prep)
+    int max_ctas;    // 0: one persistent CTA per SM; n > 0: at most n
 };
 
 struct AttnLaunch {

@@ -19,7 +19,7 @@ def test_exports_every_header_function(L):
             "qsa_score_workspace_bytes"} <= set(names)
     for n in names:
         assert hasattr(L, n), n
-    assert L.qsa_abi_version() == 2
+    assert L.qsa_abi_version() == 3
     assert L.qsa_status_str(0) == b"ok" and L.qsa_status_str(2) == b"unsupported shape"
 
 
@@ -167,3 +167,12 @@ def test_score_and_prep_head_sum_flags_rejected(L):
                       q_out=FAKE, q_out_f32=None, kq=FAKE, vq=FAKE, ksc=FAKE, vsc=FAKE, rope_k=0, qbar_out=FAKE + 16)
     s, msg = _status(L, "qsa_prep", p)
     assert s == _abi.QSA_ERR_INVALID_ARG and "qbar_out" in msg
+
+
+@pytest.mark.parametrize("fn", ["qsa_score", "qsa_score_noalloc"])
+def test_score_rejects_negative_max_ctas(L, fn):
+    a = _abi.ScoreArgs(ntok=4, pos0=10, n_q_heads=12, head_dim=128, group=32, cache_cells=100, q=FAKE, q_dtype=0,
+                       kq=FAKE, ksc=FAKE, scores=FAKE, ld=20, workspace=FAKE, workspace_bytes=1 << 20, err=None,
+                       workspace_holds_qbar=0, max_ctas=-1)
+    s, msg = _status(L, fn, a)
+    assert s == _abi.QSA_ERR_INVALID_ARG and "max_ctas" in msg

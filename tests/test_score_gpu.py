@@ -17,7 +17,7 @@ from tests.gpu_helpers import SENTINEL_BITS, assert_score_close, dev
 pytestmark = pytest.mark.gpu
 
 
-def run_gpu(q, cache, pos0, ld=None, dtype=np.float32):
+def run_gpu(q, cache, pos0, ld=None, dtype=np.float32, max_ctas=0):
     T = q.shape[0]
     C = cache.cells
     ld = ld or pos0 + T
@@ -26,7 +26,7 @@ def run_gpu(q, cache, pos0, ld=None, dtype=np.float32):
     scores = torch.full((T, ld), 0, dtype=torch.int32, device="cuda").fill_(SENTINEL_BITS).view(torch.float32)
     ws = torch.empty(qsa_score_workspace_bytes(T), dtype=torch.uint8, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    qsa_score(qd, kq, ksc, pos0, scores, ws, err=err)
+    qsa_score(qd, kq, ksc, pos0, scores, ws, err=err, max_ctas=max_ctas)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     # Untouched cells keep the sentinel: checked on the device over the whole buffer.
@@ -47,13 +47,17 @@ def _compare(q, cache, pos0, scores, rows, what, q_used=None):
 
 @pytest.mark.parametrize("T,pos0", [(1, 0), (5, 0), (70, 0), (200, 100), (130, 2050), (64, 2052), (129, 127)])
 @pytest.mark.parametrize("dtype", [np.float32, np.float16])
-def test_small_all_cells(cuda_device, T, pos0, dtype):
+@pytest.mark.parametrize("row_align", [4, 16], ids=["rows4B", "rows16B"])
+def test_small_all_cells(cuda_device, T, pos0, dtype, row_align):
+    # Two row pitches: ld = pos0 + T + 5 (rows only 4-byte aligned) and ld
+    # rounded up to a multiple of 4 floats (16-byte aligned rows).
     cache = wl.make_cache(pos0 + T, seed=31)
     dead = 3 if cache.cells > 3 else None
     if dead is not None:
         cache.ksc[dead] = 0     # a dead key: scores exactly 0
     q = wl.queries_f32(T, seed=31)
-    scores = run_gpu(q, cache, pos0, ld=pos0 + T + 5, dtype=dtype)
+    ld = pos0 + T + 5 if row_align == 4 else -(-(pos0 + T + 5) // 4) * 4
+    scores = run_gpu(q, cache, pos0, ld=ld, dtype=dtype)
     q_used = q.astype(dtype)
     _compare(q, cache, pos0, scores, np.arange(T), f"T={T} pos0={pos0} {dtype.__name__}", q_used)
     if dead is not None:
@@ -70,3 +74,16 @@ def test_full_size_sampled_rows(cuda_device, pos0):
     rng = np.random.default_rng(pos0)
     rows = np.array(sorted(set(rng.choice(T, 24, replace=False).tolist()) | {0, 63, 64, 127, 1983}))
     _compare(q, cache, pos0, scores, rows, f"T=1984 pos0={pos0}")
+
+
+@pytest.mark.parametrize("cap", [1, 3, 7, 40])
+def test_cta_cap_gives_identical_scores(cuda_device, cap):
+    # Every tile is computed the same way whichever CTA runs it, so capping the
+    # persistent grid changes only who computes what, never a bit of the output.
+    T, pos0 = 300, 2100
+    cache = wl.make_cache(pos0 + T, seed=33)
+    q = wl.queries_f32(T, seed=33)
+    base = run_gpu(q, cache, pos0)
+    capped = run_gpu(q, cache, pos0, max_ctas=cap)
+    assert torch.equal(base.view(torch.int32), capped.view(torch.int32))
+    _compare(q, cache, pos0, capped, np.array([0, 1, 127, 128, 299]), f"max_ctas={cap}")
