@@ -61,29 +61,43 @@ constexpr int NEPI = 8;      // epilogue warps 0..7 (TMEM lane quarter w % 4, to
 constexpr int NPROD = 8;     // producer warps 8..15
 constexpr int MMA_WARP = 16; // TMEM owner / MMA issuer
 constexpr int THREADS = 32 * 17;
-constexpr int CPT = TM * 8 / (NPROD * 32);  // 16-code chunks per producer thread per tile
 constexpr int PT = NPROD * 32;  // producer threads
-constexpr int NA = 2;        // A stages
-constexpr uint32_t TMEM_COLS = 256;             // two accumulators of TN fp32 columns
-constexpr uint32_t PLANE = TM * D * 2;          // one fp16 operand plane (hi or lo): 32 KB
-constexpr uint32_t KBLOCK = TM * 128;           // bytes of one 64-wide K block of a plane
-static_assert(TM == TN, "A and B planes share one geometry");
-constexpr uint32_t A_STAGE = 2 * PLANE;         // key hi + lo
-constexpr uint32_t OFF_B = NA * A_STAGE;        // qbar hi + lo of one token tile
-constexpr uint32_t OFF_BAR = OFF_B + 2 * PLANE;
-constexpr uint32_t OFF_FLAG = OFF_BAR + (2 * NA + 6) * 8;
+constexpr int NA = 2;        // A stages (in tensor memory)
+// Tensor memory: two fp32 accumulators of TN columns, then NA key stages of
+// D/2 hi columns and D/2 lo columns (two fp16 per 32-bit column, lane = cell).
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t A_COL = 2 * TN;
+constexpr uint32_t A_STAGE_COLS = D;
+static_assert(A_COL + NA * A_STAGE_COLS <= TMEM_COLS, "tensor memory layout");
+constexpr uint32_t PLANE = TN * D * 2;          // one fp16 qbar plane (hi or lo) in shared memory: 32 KB
+constexpr uint32_t KBLOCK = TN * 128;           // bytes of one 64-wide K block of a plane
+constexpr uint32_t B_PAIR = 2 * PLANE;          // qbar hi + lo of one token tile
+constexpr uint32_t OFF_BAR = 2 * B_PAIR;        // two token tiles in flight
+constexpr uint32_t OFF_FLAG = OFF_BAR + (2 * NA + 8) * 8;
 constexpr uint32_t SMEM_USED = OFF_FLAG + 16;
-// The layout needs more than half of an SM's shared memory, so exactly one
-// CTA (and one tensor-memory allocation) lives on each SM.
+// All 512 tensor-memory columns and more than half of the shared memory: one
+// CTA per SM.
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory layout");
+// A second CTA on the SM would wait for tensor-memory columns the first holds.
+static_assert(2 * SMEM_ALLOC > 227 * 1024, "one CTA per SM");
 
 using namespace tc;
 
 // Instruction descriptor of the score tile: M = 128 cells, N = 128 tokens,
 // fp16 operands (both K-major), fp32 accumulation.
 constexpr uint32_t IDESC = idesc_f16(TM, TN, false, false);
+
+// D (tensor memory) (+)= A (tensor memory, lane = row, two fp16 of K per
+// 32-bit column) x B (shared-memory descriptor).
+__device__ __forceinline__ void mma_f16_ts(uint32_t dtmem, uint32_t atmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(dtmem),
+        "r"(atmem), "l"(bdesc), "r"(idesc), "r"(acc));
+}
 
 // --- kernels ----------------------------------------------------------------
 
@@ -190,9 +204,9 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a) {
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gen = smem_raw + (base - raw);
-    const uint32_t sA = base, sB = base + OFF_B, bar = base + OFF_BAR;
-    const uint32_t a_full = bar, a_empty = bar + 8 * NA, b_full = bar + 16 * NA, b_empty = b_full + 8,
-                   acc_full = b_empty + 8, acc_empty = acc_full + 16;
+    const uint32_t sB = base, bar = base + OFF_BAR;
+    const uint32_t a_full = bar, a_empty = bar + 8 * NA, b_full = bar + 16 * NA, b_empty = b_full + 16,
+                   acc_full = b_empty + 16, acc_empty = acc_full + 16;
     volatile int *abort = reinterpret_cast<volatile int *>(gen + OFF_FLAG);
     volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gen + OFF_FLAG + 8);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -202,9 +216,9 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a) {
             mbar_init(a_full + 8 * i, PT);
             mbar_init(a_empty + 8 * i, 1);
         }
-        mbar_init(b_full, PT);  // one cp.async-tracked arrival per producer thread
-        mbar_init(b_empty, 1);
         for (int i = 0; i < 2; ++i) {
+            mbar_init(b_full + 8 * i, PT);  // one cp.async-tracked arrival per producer thread
+            mbar_init(b_empty + 8 * i, 1);
             mbar_init(acc_full + 8 * i, 1);
             mbar_init(acc_empty + 8 * i, NEPI * 32);
         }
@@ -237,81 +251,78 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a) {
 
     if (warp >= NEPI && warp < NEPI + NPROD) {
         // ---- producers ----
-        // Thread pt converts, per tile, 16-code chunks q = it*PT + pt: row
-        // m = q / 8 (a cell), dims 16*(q % 8) .. +15, all in scale group
-        // (q % 8) / 2.
-        const int pt = tid - NEPI * 32;
+        // Producer warp p (0..7) owns tensor-memory lane quarter p % 4 and
+        // dims 64(p / 4) .. +63: each thread converts one cell's 64 codes
+        // (two scale groups) into 32 hi and 32 lo columns of the A stage.
+        const int pt = tid - NEPI * 32, pw = warp - NEPI, quarter = pw & 3, kh = pw >> 2;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         Walker w = w0;
         int nb = 0, cur_tt = -1;
-        uint4 pre[CPT];
-        uint2 psc[CPT];
+        uint4 pre[4];
+        uint2 psc;
         auto load_a = [&](int ct) {
+            const int c = ct * TM + row;
+            const bool ok = c < a.cache_cells;
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.kq + (size_t)c * D + kh * 64);
 #pragma unroll
-            for (int it = 0; it < CPT; ++it) {
-                const int q = it * PT + pt, m = q >> 3, dc = q & 7;
-                const int c = ct * TM + m;
-                const bool ok = c < a.cache_cells;
-                pre[it] = ok ? __ldg(reinterpret_cast<const uint4 *>(a.kq + (size_t)c * D) + dc)
-                             : make_uint4(0u, 0u, 0u, 0u);
-                psc[it] = ok ? __ldg(reinterpret_cast<const uint2 *>(a.ksc + (size_t)c * 4)) : make_uint2(0u, 0u);
-            }
+            for (int i = 0; i < 4; ++i) pre[i] = ok ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+            psc = ok ? __ldg(reinterpret_cast<const uint2 *>(a.ksc + (size_t)c * 4)) : make_uint2(0u, 0u);
         };
         if (n > 0) load_a(w.ct);
         for (int k = 0; k < n; ++k) {
             if (w.tt != cur_tt) {
                 // qbar hi/lo rows of the new token tile (rows past ntok read
-                // as zero) into the B buffer, completing on b_full; the MMAs
-                // of the previous token tile must have finished reading it.
-                if (nb >= 1 && !mbar_wait_or_abort(b_empty, (nb - 1) & 1, abort)) break;
+                // as zero) into one of two B buffers, completing on b_full.
+                const int bs = nb & 1;
+                if (nb >= 2 && !mbar_wait_or_abort(b_empty + 8 * bs, ((nb >> 1) - 1) & 1, abort)) break;
+                const uint32_t dstB = sB + bs * B_PAIR;
 #pragma unroll 4
                 for (int it = 0; it < 2 * TN * 16 / PT; ++it) {
-                    const int q = it * PT + pt, part = q / (TN * 16), row = (q / 16) % TN, u = q & 15;
-                    const int t = w.tt * TN + row;
+                    const int q = it * PT + pt, part = q / (TN * 16), r = (q / 16) % TN, u = q & 15;
+                    const int t = w.tt * TN + r;
                     const bool ok = t < a.ntok;
-                    cp_async16_zfill(sB + part * PLANE + plane_off(row, u),
+                    cp_async16_zfill(dstB + part * PLANE + plane_off(r, u),
                                      reinterpret_cast<const uint4 *>(a.qsum + ((size_t)(ok ? t : 0) * 2 + part) * D) + u,
                                      ok ? 16u : 0u);
                 }
-                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(b_full) : "memory");
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(b_full + 8 * bs)
+                             : "memory");
                 ++nb;
                 cur_tt = w.tt;
             }
             const int st = k % NA;
             if (k >= NA && !mbar_wait_or_abort(a_empty + 8 * st, ((k / NA) - 1) & 1, abort)) break;
-            const uint32_t dst = sA + st * A_STAGE;
+            fence_after();
+            const float p2 = pow2f(cell_exponent(psc));
+            const uint32_t graw = kh ? psc.y : psc.x;  // this thread's two scale groups
+            const __half2 sg[2] = {scaled_scale(graw & 0xFFFFu, p2), scaled_scale(graw >> 16, p2)};
+            const uint32_t col = lane_base + A_COL + st * A_STAGE_COLS + kh * 32;
 #pragma unroll
-            for (int it = 0; it < CPT; ++it) {
-                const int q = it * PT + pt, m = q >> 3, dc = q & 7;
-                const float p2 = pow2f(cell_exponent(psc[it]));
-                const uint32_t raw16 = (dc >> 2) ? (dc & 2 ? psc[it].y >> 16 : psc[it].y & 0xFFFFu)
-                                                 : (dc & 2 ? psc[it].x >> 16 : psc[it].x & 0xFFFFu);
-                const __half2 s2 = scaled_scale(raw16, p2);
-                uint32_t h[8];
-                codes_to_h2(pre[it].x ^ 0x80808080u, h[0], h[1]);
-                codes_to_h2(pre[it].y ^ 0x80808080u, h[2], h[3]);
-                codes_to_h2(pre[it].z ^ 0x80808080u, h[4], h[5]);
-                codes_to_h2(pre[it].w ^ 0x80808080u, h[6], h[7]);
-                uint32_t hi[8], lo[8];
+            for (int g = 0; g < 2; ++g) {  // one 32-dim group: 16 hi and 16 lo columns
+                uint32_t h[16], hi[16], lo[16];
+                codes_to_h2(pre[2 * g].x ^ 0x80808080u, h[0], h[1]);
+                codes_to_h2(pre[2 * g].y ^ 0x80808080u, h[2], h[3]);
+                codes_to_h2(pre[2 * g].z ^ 0x80808080u, h[4], h[5]);
+                codes_to_h2(pre[2 * g].w ^ 0x80808080u, h[6], h[7]);
+                codes_to_h2(pre[2 * g + 1].x ^ 0x80808080u, h[8], h[9]);
+                codes_to_h2(pre[2 * g + 1].y ^ 0x80808080u, h[10], h[11]);
+                codes_to_h2(pre[2 * g + 1].z ^ 0x80808080u, h[12], h[13]);
+                codes_to_h2(pre[2 * g + 1].w ^ 0x80808080u, h[14], h[15]);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 16; ++j) {
                     // hi = fp16(k * s); lo = fp16(k * s - hi), one rounding (fused).
                     const __half2 kk = *reinterpret_cast<const __half2 *>(&h[j]);
-                    const __half2 vh = __hmul2(kk, s2);
-                    const __half2 vl = __hfma2(kk, s2, __hneg2(vh));
+                    const __half2 vh = __hmul2(kk, sg[g]);
+                    const __half2 vl = __hfma2(kk, sg[g], __hneg2(vh));
                     hi[j] = *reinterpret_cast<const uint32_t *>(&vh);
                     lo[j] = *reinterpret_cast<const uint32_t *>(&vl);
                 }
-                const uint32_t o0 = plane_off(m, 2 * dc), o1 = plane_off(m, 2 * dc + 1);
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst + o0), "r"(hi[0]), "r"(hi[1]),
-                             "r"(hi[2]), "r"(hi[3]));
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst + o1), "r"(hi[4]), "r"(hi[5]),
-                             "r"(hi[6]), "r"(hi[7]));
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst + PLANE + o0), "r"(lo[0]),
-                             "r"(lo[1]), "r"(lo[2]), "r"(lo[3]));
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst + PLANE + o1), "r"(lo[4]),
-                             "r"(lo[5]), "r"(lo[6]), "r"(lo[7]));
+                tmem_st16(col + g * 16, hi);
+                tmem_st16(col + D / 2 + g * 16, lo);
             }
-            fence_async_smem();
+            tmem_wait_st();
+            fence_before();
             mbar_arrive(a_full + 8 * st);
             walk_next(a, w);
             if (k + 1 < n) load_a(w.ct);
@@ -321,10 +332,11 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a) {
         // ---- MMA issuer ----
         if (lane == 0) {
             Walker w = w0;
-            int nb = 0, cur_tt = -1;
+            int nb = 0, cur_tt = -1, bs = 0;
             for (int k = 0; k < n; ++k) {
                 if (w.tt != cur_tt) {
-                    if (!mbar_wait_or_abort(b_full, nb & 1, abort)) break;
+                    bs = nb & 1;
+                    if (!mbar_wait_or_abort(b_full + 8 * bs, (nb >> 1) & 1, abort)) break;
                     ++nb;
                     cur_tt = w.tt;
                 }
@@ -332,22 +344,23 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a) {
                 if (!mbar_wait_or_abort(a_full + 8 * st, (k / NA) & 1, abort)) break;
                 if (k >= 2 && !mbar_wait_or_abort(acc_empty + 8 * b, ((k >> 1) - 1) & 1, abort)) break;
                 fence_after();
-                const uint64_t ah = sw128_kmajor(sA + st * A_STAGE), al = sw128_kmajor(sA + st * A_STAGE + PLANE);
-                const uint64_t bh = sw128_kmajor(sB), bl = sw128_kmajor(sB + PLANE);
+                const uint32_t ah = tmem + A_COL + st * A_STAGE_COLS, al = ah + D / 2;
+                const uint64_t bh = sw128_kmajor(sB + bs * B_PAIR), bl = sw128_kmajor(sB + bs * B_PAIR + PLANE);
                 const uint32_t dt = tmem + (uint32_t)(b * TN);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    // k-step ks: dims 16ks..16ks+15, in K block ks / 4 at byte 32 (ks % 4).
+                    // k-step ks: dims 16ks..16ks+15 -- A columns 8ks..8ks+7, B K block
+                    // ks / 4 at byte 32 (ks % 4).
                     const uint64_t koff = (uint64_t)(((ks >> 2) * KBLOCK + (ks & 3) * 32) >> 4);
-                    mma_f16(dt, ah + koff, bh + koff, IDESC, ks ? 1u : 0u);
-                    mma_f16(dt, ah + koff, bl + koff, IDESC, 1u);
-                    mma_f16(dt, al + koff, bh + koff, IDESC, 1u);
+                    mma_f16_ts(dt, ah + 8 * ks, bh + koff, IDESC, ks ? 1u : 0u);
+                    mma_f16_ts(dt, ah + 8 * ks, bl + koff, IDESC, 1u);
+                    mma_f16_ts(dt, al + 8 * ks, bh + koff, IDESC, 1u);
                 }
                 mma_commit(a_empty + 8 * st);
                 mma_commit(acc_full + 8 * b);
                 Walker nx = w;
                 walk_next(a, nx);
-                if (k + 1 == n || nx.tt != w.tt) mma_commit(b_empty);
+                if (k + 1 == n || nx.tt != w.tt) mma_commit(b_empty + 8 * bs);
                 w = nx;
             }
         }
