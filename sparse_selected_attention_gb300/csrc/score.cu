@@ -367,9 +367,8 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a) {
     } else if (warp < NEPI) {
         // ---- epilogue ----
         // Thread (warp w, lane l) holds cell c0 + 32(w % 4) + l and token
-        // columns 64(w / 4) .. +63.  It drains them in two 32-column pieces,
-        // the second piece's tensor-memory load issued before the first piece
-        // is stored, and scales by 2^-e_c.  Fully causal tiles store without
+        // columns 64(w / 4) .. +63, loaded as two 32-column pieces, scales
+        // them by 2^-e_c and stores them.  Fully causal tiles store without
         // per-element tests.  For a fixed column the warp's 32
         // lanes store 32 consecutive cells of one score row.
         const int quarter = warp & 3, half = warp >> 2;
@@ -419,13 +418,15 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a) {
                     }
                 }
             };
+            // Both loads, then the accumulator is released before any store,
+            // so that the MMAs of the tile after next can start.
             tmem_ld32(tbase, va);
-            wait32(va);
             tmem_ld32(tbase + 32, vb);
-            store32(va, 0);
+            wait32(va);
             wait32(vb);
             fence_before();
             mbar_arrive(acc_empty + 8 * b);
+            store32(va, 0);
             store32(vb, 32);
             w = nx;
             kv = kv_next;
