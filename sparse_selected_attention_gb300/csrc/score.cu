@@ -31,18 +31,20 @@
 // (token tile, cell tile) pairs, 128 x 128 each, and runs it as a
 // warp-specialised pipeline:
 //  - eight producer warps turn a cell tile's int8 codes and scales into the
-//    hi and lo key planes of one of two A stages, and copy qbar hi/lo of 128
-//    tokens into the B buffer when the token tile changes;
+//    hi and lo key planes of one of two A stages in TENSOR memory (lane =
+//    cell, two fp16 per 32-bit column, written with tcgen05.st), and copy
+//    qbar hi/lo of 128 tokens into one of two shared-memory B buffers
+//    (128-byte-swizzled K-major) when the token tile changes;
 //  - one thread issues 8 k-steps x 3 tcgen05.mma (M = 128 cells, N = 128
-//    tokens, K = 16) into one of two accumulators in tensor memory
-//    (2 x 128 columns);
+//    tokens, K = 16; A read from tensor memory, B through a shared-memory
+//    descriptor) into one of two accumulators in tensor memory (2 x 128
+//    columns);
 //  - eight epilogue warps drain the other accumulator: each thread holds one
 //    cell and 64 token columns, so every store instruction writes 32
 //    consecutive cells of one score row (128 bytes).
-// Operands use the 128-byte-swizzled K-major layout read through
-// shared-memory descriptors.  Every mbarrier wait is bounded; on expiry the
-// kernel records QSA_DEVERR_TIMEOUT, all roles stop, tensor memory is freed
-// and the kernel returns.
+// Every mbarrier wait is bounded; on expiry the kernel records
+// QSA_DEVERR_TIMEOUT, all roles stop, tensor memory is freed and the kernel
+// returns.
 #include <cuda_fp16.h>
 
 #include <mutex>

@@ -87,3 +87,23 @@ def test_cta_cap_gives_identical_scores(cuda_device, cap):
     capped = run_gpu(q, cache, pos0, max_ctas=cap)
     assert torch.equal(base.view(torch.int32), capped.view(torch.int32))
     _compare(q, cache, pos0, capped, np.array([0, 1, 127, 128, 299]), f"max_ctas={cap}")
+
+
+@pytest.mark.parametrize("ratio", [1e2, 1e4, 3e5])
+def test_mixed_group_scales(cuda_device, ratio):
+    # The kernel folds each cell's four group scales into its codes under one
+    # power of two per cell, set by the largest scale; a much smaller group
+    # then sits low in fp16's range.  Cells here mix groups whose scales differ
+    # by `ratio` (the quantiser's own scales are a group's amax / 127), and
+    # some cells have a zero group or only their smallest group non-zero.
+    T, pos0 = 96, 1000
+    cache = wl.make_cache(pos0 + T, seed=35)
+    s = cache.ksc.view(np.float16).astype(np.float32)
+    s[:, 1] = s[:, 0] / ratio
+    s[::3, 2] = 0.0
+    s[1::5, 0] = 0.0
+    s[1::5, 2:] = 0.0            # only group 1 (the small one) left
+    cache.ksc[...] = s.astype(np.float16).view(cache.ksc.dtype)
+    q = wl.queries_f32(T, seed=35)
+    scores = run_gpu(q, cache, pos0)
+    _compare(q, cache, pos0, scores, np.arange(T), f"group scale ratio {ratio:g}")
