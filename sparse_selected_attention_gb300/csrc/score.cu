@@ -160,6 +160,13 @@ __device__ __forceinline__ __half2 scaled_scale(uint32_t raw16, float p2) {
     return __halves2half2(h, h);
 }
 
+// Eight consecutive 32-bit columns of tensor memory for the warp's 32 lanes.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 // Thirty-two consecutive 32-bit columns of tensor memory for the warp's 32 lanes.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile(
@@ -201,7 +208,9 @@ __device__ __forceinline__ uint32_t plane_off(int r, int u) {
 // tensor memory and one of its threads issues the MMAs.  Stages are handed
 // over with mbarriers: a_full / a_empty (NA A stages), b_full / b_empty (the
 // B buffer), acc_full / acc_empty (2 TMEM accumulators).
-__global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a) {
+// 72 registers a thread (544 x 72 = 39 K a CTA, no spills): a score CTA then
+// leaves room on its SM for one attention CTA.
+__global__ void __maxnreg__(72) score_kernel(ScoreLaunch a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -301,27 +310,23 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a) {
             const __half2 sg[2] = {scaled_scale(graw & 0xFFFFu, p2), scaled_scale(graw >> 16, p2)};
             const uint32_t col = lane_base + A_COL + st * A_STAGE_COLS + kh * 32;
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {  // one 32-dim group: 16 hi and 16 lo columns
-                uint32_t h[16], hi[16], lo[16];
-                codes_to_h2(pre[2 * g].x ^ 0x80808080u, h[0], h[1]);
-                codes_to_h2(pre[2 * g].y ^ 0x80808080u, h[2], h[3]);
-                codes_to_h2(pre[2 * g].z ^ 0x80808080u, h[4], h[5]);
-                codes_to_h2(pre[2 * g].w ^ 0x80808080u, h[6], h[7]);
-                codes_to_h2(pre[2 * g + 1].x ^ 0x80808080u, h[8], h[9]);
-                codes_to_h2(pre[2 * g + 1].y ^ 0x80808080u, h[10], h[11]);
-                codes_to_h2(pre[2 * g + 1].z ^ 0x80808080u, h[12], h[13]);
-                codes_to_h2(pre[2 * g + 1].w ^ 0x80808080u, h[14], h[15]);
+            for (int i = 0; i < 4; ++i) {  // 16 codes (half a scale group): 8 hi and 8 lo columns
+                uint32_t h[8], hi[8], lo[8];
+                codes_to_h2(pre[i].x ^ 0x80808080u, h[0], h[1]);
+                codes_to_h2(pre[i].y ^ 0x80808080u, h[2], h[3]);
+                codes_to_h2(pre[i].z ^ 0x80808080u, h[4], h[5]);
+                codes_to_h2(pre[i].w ^ 0x80808080u, h[6], h[7]);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
+                for (int j = 0; j < 8; ++j) {
                     // hi = fp16(k * s); lo = fp16(k * s - hi), one rounding (fused).
                     const __half2 kk = *reinterpret_cast<const __half2 *>(&h[j]);
-                    const __half2 vh = __hmul2(kk, sg[g]);
-                    const __half2 vl = __hfma2(kk, sg[g], __hneg2(vh));
+                    const __half2 vh = __hmul2(kk, sg[i >> 1]);
+                    const __half2 vl = __hfma2(kk, sg[i >> 1], __hneg2(vh));
                     hi[j] = *reinterpret_cast<const uint32_t *>(&vh);
                     lo[j] = *reinterpret_cast<const uint32_t *>(&vl);
                 }
-                tmem_st16(col + g * 16, hi);
-                tmem_st16(col + D / 2 + g * 16, lo);
+                tmem_st8(col + 8 * i, hi);
+                tmem_st8(col + D / 2 + 8 * i, lo);
             }
             tmem_wait_st();
             fence_before();
@@ -398,38 +403,40 @@ __global__ void __launch_bounds__(THREADS, 1) score_kernel(ScoreLaunch a) {
             if (!mbar_wait_or_abort(acc_full + 8 * b, (k >> 1) & 1, abort)) break;
             fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * TN + half * (TN / 2));
-            uint32_t va[32], vb[32];
-            auto wait32 = [&](uint32_t (&v)[32]) {
+            uint32_t va[16], vb[16];
+            auto wait16 = [&]() {
                 tmem_wait_ld();
                 // Each loaded register passes through an empty volatile
                 // statement, so no use of it can move above the wait.
 #pragma unroll
-                for (int j = 0; j < 32; ++j) asm volatile("" : "+r"(v[j]));
+                for (int j = 0; j < 16; ++j) asm volatile("" : "+r"(va[j]), "+r"(vb[j]));
             };
             // Streaming stores: the scores are not read again by this pass.
-            auto store32 = [&](const uint32_t (&v)[32], int j0) {
+            auto store16 = [&](const uint32_t (&v)[16], int j0) {
                 float *p = col + (size_t)j0 * a.ld;
                 if (full) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j, p += a.ld) __stcs(p, fmaf(__uint_as_float(v[j]), inv, 0.0f));
+                    for (int j = 0; j < 16; ++j, p += a.ld) __stcs(p, fmaf(__uint_as_float(v[j]), inv, 0.0f));
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j, p += a.ld) {
+                    for (int j = 0; j < 16; ++j, p += a.ld) {
                         const int t = tw + j0 + j;
                         if (t < a.ntok && t >= tmin) __stcs(p, fmaf(__uint_as_float(v[j]), inv, 0.0f));
                     }
                 }
             };
-            // Both loads, then the accumulator is released before any store,
-            // so that the MMAs of the tile after next can start.
-            tmem_ld32(tbase, va);
-            tmem_ld32(tbase + 32, vb);
-            wait32(va);
-            wait32(vb);
+            tmem_ld16(tbase, va);
+            tmem_ld16(tbase + 16, vb);
+            wait16();
+            store16(va, 0);
+            store16(vb, 16);
+            tmem_ld16(tbase + 32, va);
+            tmem_ld16(tbase + 48, vb);
+            wait16();
             fence_before();
             mbar_arrive(acc_empty + 8 * b);
-            store32(va, 0);
-            store32(vb, 32);
+            store16(va, 32);
+            store16(vb, 48);
             w = nx;
             kv = kv_next;
         }
