@@ -120,8 +120,8 @@ typedef struct {
  * already filled it through qsa_prep's qbar_out for the same tokens, q is
  * ignored (it may be NULL) and the head-sum pass is skipped; the scores are
  * bit-identical to those computed from the fp32 q_out_f32 of that prep.
- * max_ctas: 0 runs one persistent CTA per SM (each CTA takes a whole SM's
- * shared memory); n > 0 runs at most n.  A caller that overlaps the score with
+ * max_ctas: 0 runs one persistent CTA per SM (each CTA takes all of an SM's
+ * tensor memory); n > 0 runs at most n.  A caller that overlaps the score with
  * other kernels on another stream caps it so that those kernels keep the
  * remaining SMs; the scores do not depend on the cap.  Negative is rejected.
  * Requires pos0 + ntok <= cache_cells.  Supported: head_dim == 128,
