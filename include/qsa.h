@@ -124,6 +124,13 @@ typedef struct {
  * tensor memory); n > 0 runs at most n.  A caller that overlaps the score with
  * other kernels on another stream caps it so that those kernels keep the
  * remaining SMs; the scores do not depend on the cap.  Negative is rejected.
+ * Range: the head sum travels as an unscaled fp16 pair hi + lo.  Each
+ * |qbar[t,d]| must stay below 65504 (beyond, it overflows to inf), and an
+ * element's representation error is at most 2^-22 of it or 2^-25 absolute,
+ * whichever is larger.  So the scores meet 1e-4 * sum|terms| for query values
+ * of about 1e-3 and up -- every row out of qsa_prep with norm weights of
+ * order one, whose head sums stay below a few hundred -- and lose relative
+ * accuracy for rows of much smaller values.
  * Requires pos0 + ntok <= cache_cells.  Supported: head_dim == 128,
  * group == 32, 1 <= n_q_heads <= 64.  q, kq 16-byte aligned; ksc 8-byte.
  */

@@ -107,3 +107,17 @@ def test_mixed_group_scales(cuda_device, ratio):
     q = wl.queries_f32(T, seed=35)
     scores = run_gpu(q, cache, pos0)
     _compare(q, cache, pos0, scores, np.arange(T), f"group scale ratio {ratio:g}")
+
+
+@pytest.mark.parametrize("mag", [3e-3, 2e3])
+def test_query_magnitudes_in_range(cuda_device, mag):
+    # The head sum travels as an unscaled fp16 hi/lo pair.  Near both ends of
+    # its stated range -- query values of a few 1e-3 (the lo parts partly
+    # subnormal) and head sums up to about 3e4 (fp16 tops out at 65504) --
+    # the scores still meet the 1e-4 A bound.
+    T, pos0 = 70, 300
+    cache = wl.make_cache(pos0 + T, seed=37)
+    q = (wl.queries_f32(T, seed=37) * np.float32(mag)).astype(np.float32)
+    scores = run_gpu(q, cache, pos0)
+    assert bool(torch.isfinite(scores[0, : pos0 + 1]).all())
+    _compare(q, cache, pos0, scores, np.arange(T), f"query magnitude {mag:g}")
