@@ -76,7 +76,9 @@ def parse():
                    help="SMs the overlapped score takes (0: it fills the attention's tail instead)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--cpu-sample-seconds", type=float, default=15.0)
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the per-workload block (decode windows, short prompt, score sweep)")
+    p.add_argument("--cpu-sample-seconds", type=float, default=8.0)
     return p.parse_args()
 
 
@@ -229,47 +231,85 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle, as it stands, on a bounded sample
 # ---------------------------------------------------------------------------
+#
+# The oracle runs in a pool of single-threaded worker processes (started with
+# `spawn`, so no worker inherits the parent's CUDA state).  Each worker makes
+# the workload's inputs once; a task is a list of token rows, for which it
+# runs prep on those rows, their score rows over every causal cell and their
+# attention, and returns its own compute time.
 
-CPU_SAMPLE_CODE = r"""
-import json, math, sys, time
-sys.path.insert(0, ROOT)
-import numpy as np
-from oracle import attention, prep, score
-from sparse_selected_attention_gb300 import workloads as wl
-n = NSAMP
-T, pos0 = 1984, 30000
-inp = wl.prep_inputs(T, seed=5)
-cache = wl.make_cache(pos0 + T, seed=5)
-ids = wl.even_ids(T, pos0)
-rows = np.linspace(0, T - 1, n).astype(np.int64)
-t0 = time.perf_counter()
-q64, q16, q32 = prep(inp.q_in[rows], inp.k_in[rows], inp.v_in[rows], inp.norm_w, pos0, cache.kq, cache.vq,
-                     cache.ksc, cache.vsc)
-S = score(q32, cache.kq, cache.ksc, pos0)
-o = attention(q16, cache.kq, cache.vq, cache.ksc, cache.vsc, ids[rows], 1 / math.sqrt(128))
-dt = time.perf_counter() - t0
-print(json.dumps({"tokens": n, "seconds": dt}))
-"""
+_ORACLE = None
 
 
-def run_cpu_sample(nsamp):
-    code = CPU_SAMPLE_CODE.replace("ROOT", repr(ROOT)).replace("NSAMP", str(nsamp))
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
-    if r.returncode != 0:
-        raise RuntimeError(r.stderr[-2000:])
-    return json.loads(r.stdout.strip().splitlines()[-1])
+def _oracle_worker_init(ntok, pos0, width):
+    os.environ.update(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    sys.path.insert(0, ROOT)
+    from sparse_selected_attention_gb300 import workloads as wl
+    global _ORACLE
+    _ORACLE = {"inp": wl.prep_inputs(ntok, seed=5), "cache": wl.make_cache(pos0 + ntok, seed=5),
+               "ids": wl.even_ids(ntok, pos0, width), "pos0": pos0}
 
 
-def cpu_baseline(target_seconds):
-    probe = run_cpu_sample(4)
-    per_tok = probe["seconds"] / 4
-    n = int(max(4, min(1984, target_seconds / max(per_tok, 1e-6))))
-    res = run_cpu_sample(n)
-    return {"value": res["tokens"] / res["seconds"], "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{res['tokens']} evenly spaced token rows of the workload (prep of their rows, their "
-                      f"score rows over all causal cells, their attention), {res['seconds']:.1f} s, one thread"}
+def _oracle_rows(rows):
+    import numpy as np
+
+    from oracle import attention, prep, score
+    w = _ORACLE
+    inp, cache, rows = w["inp"], w["cache"], np.asarray(rows, dtype=np.int64)
+    t0 = time.perf_counter()
+    q64, q16, q32 = prep(inp.q_in[rows], inp.k_in[rows], inp.v_in[rows], inp.norm_w, w["pos0"], cache.kq,
+                         cache.vq, cache.ksc, cache.vsc)
+    score(q32, cache.kq, cache.ksc, w["pos0"])
+    attention(q16, cache.kq, cache.vq, cache.ksc, cache.vsc, w["ids"][rows], 1 / math.sqrt(128))
+    return len(rows), time.perf_counter() - t0
+
+
+class OraclePool:
+    """`cores` single-threaded oracle workers on this host."""
+
+    def __init__(self, cores, ntok=NTOK, pos0=POS0):
+        import multiprocessing as mp
+        from concurrent.futures import ProcessPoolExecutor
+        self.cores, self.ntok = cores, ntok
+        self.ex = ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn"),
+                                      initializer=_oracle_worker_init, initargs=(ntok, pos0, WIDTH))
+        list(self.ex.map(_oracle_rows, [[0]] * cores))  # start every worker and warm it
+
+    def rows(self, n, offset=0):
+        """n token rows spread evenly over the workload, starting at an offset."""
+        return [int((offset + i * self.ntok / n)) % self.ntok for i in range(n)]
+
+    def run(self, rows, workers):
+        """Rows dealt to `workers` workers at once; (rows done, wall seconds)."""
+        parts = [rows[i::workers] for i in range(workers)]
+        t0 = time.perf_counter()
+        done = sum(n for n, _ in self.ex.map(_oracle_rows, parts))
+        return done, time.perf_counter() - t0
+
+    def close(self):
+        self.ex.shutdown()
+
+
+def cpu_baseline(target_seconds, pool=None):
+    """The oracle's throughput on one thread and on every host core, each
+    over a sample of about `target_seconds`."""
+    own = pool is None
+    pool = pool or OraclePool(os.cpu_count() or 1)
+    try:
+        n, dt = pool.run(pool.rows(4), 1)
+        per_row = dt / n
+        n1 = int(max(4, min(NTOK, target_seconds / per_row)))
+        d1, t1 = pool.run(pool.rows(n1), 1)
+        nc = int(max(pool.cores, min(NTOK, target_seconds * pool.cores / per_row)))
+        dc, tc = pool.run(pool.rows(nc, offset=1), pool.cores)
+    finally:
+        if own:
+            pool.close()
+    return {"value": dc / tc, "unit": UNIT, "cores": pool.cores, "kind": "oracle",
+            "single_thread_value": d1 / t1,
+            "sample": f"{dc} evenly spaced token rows of the workload on {pool.cores} single-threaded worker "
+                      f"processes ({tc:.1f} s wall); each row: prep of its q/k/v rows, its score row over all "
+                      f"causal cells, its attention over its ids.  One thread: {d1} rows in {t1:.1f} s"}
 
 
 # ---------------------------------------------------------------------------
@@ -476,12 +516,139 @@ def run_ours(args, rank, world, local_rank):
     kernels["score"]["pairs"] = score_pairs(T, pos0)
     if not args.select:
         kernels["score"]["overlapped_with"] = "attn (second stream; avg_ms includes waiting for SMs)"
-    # The 12-head formula's contraction, 2*12*128 flops per causal pair; the
-    # kernel sums the heads first, so its tensor pipe does a twelfth of it.
-    kernels["score"]["tflops_algorithmic"] = 2 * HQ * D * score_pairs(T, pos0) / (own["score"] / 1e3) / 1e12
+    # The score's tensor-core work as issued (three fp16 128x128x128 products
+    # per tile over the head-summed queries), and the bytes it moves; the
+    # kernel is bound by its fp32 score writes, not by the tensor pipe.
+    tc, tc_src = bf16_peak()
+    ex = score_flops_executed(T, pos0) / (own["score"] / 1e3) / 1e12
+    kernels["score"].update(tensor_tflops_executed=ex, frac_of_f16_peak_executed=ex / tc, f16_peak_source=tc_src,
+                            frac_of_hbm_peak=kernels["score"]["achieved_gbs"] / peaks()[0])
     kernels["attn"]["valid_cells"] = valid
     return {"ms": ms, "wall_s": wall, "e2e": e2e, "clocks": clocks, "roofline": roof, "kernels": kernels,
             "launches_per_step": 4 if args.select else 3}  # prep, score, (select,) attention
+
+
+def score_tiles(ntok, pos0, tm=128, tn=128):
+    """128 x 128 (cell, token) tiles the score kernel runs: per 128-token
+    tile, every cell tile up to its last token's causal bound."""
+    tiles = 0
+    for t0 in range(0, ntok, tn):
+        tiles += (pos0 + min(ntok - 1, t0 + tn - 1)) // tm + 1
+    return tiles
+
+
+def score_flops_executed(ntok, pos0):
+    """Tensor-core flops the score kernel issues: three 128x128x128 fp16
+    products (hi*hi, hi*lo, lo*hi) per tile."""
+    return score_tiles(ntok, pos0) * 3 * 2 * 128 ** 3
+
+
+def bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        return 1900.0, "fallback 1.9 PFLOP/s"
+
+
+def _device_times(stream, fn, n, flush=None):
+    """Device time of each of n calls of fn on `stream` (ms), L2 flushed
+    before each call when `flush` is given (outside the call's events)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        if flush is not None:
+            flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sorted(a.elapsed_time(b) for a, b in evs)
+
+
+def run_configs(dev, n):
+    """Every workload the method is specified on, timed in the same run:
+    the two decode windows (fused and split attention, L2 cold and warm),
+    the short and long prompt attention, and the score sweep."""
+    import numpy as np
+    import torch
+
+    from sparse_selected_attention_gb300 import qsa_attn, qsa_score, qsa_score_workspace_bytes
+    from sparse_selected_attention_gb300 import workloads as wl
+
+    def to(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    hbm, hbm_src = peaks()
+    tc, tc_src = bf16_peak()
+    med = lambda t: t[len(t) // 2]
+    out = {"peaks": {"hbm_gbs": hbm, "hbm_source": hbm_src, "f16_tflops": tc,
+                     "f16_source": tc_src + " (fp16 and bf16 run at the same dense rate)"},
+           "calls_per_point": n}
+
+    def attn_case(w):
+        cache = wl.make_cache(w.cells, seed=w.seed)
+        kq, vq, ksc, vsc = (to(x) for x in (cache.kq, cache.vq, cache.ksc, cache.vsc))
+        q = to(wl.queries_f16(w.ntok, seed=w.seed))
+        ids_np = w.make_ids()
+        ids = to(ids_np)
+        o = torch.empty((w.ntok, HQ, D), dtype=torch.float16, device=dev)
+        part = torch.empty((w.ntok, w.width // 64, HQ, D + 2), dtype=torch.float32, device=dev)
+        fused = lambda: qsa_attn(q, kq, vq, ksc, vsc, ids, o)
+        split = lambda: qsa_attn(q, kq, vq, ksc, vsc, ids, o, part=part)
+        ab, valid = attn_bytes(ids_np, w.ntok)
+        return fused, split, ab, valid
+
+    for key, w in (("0_tiny_decode", wl.TINY_DECODE), ("1_mtp_decode", wl.MTP_DECODE)):
+        fused, split, ab, valid = attn_case(w)
+        rec = {"workload": w.name, "valid_cells": valid, "algorithmic_bytes": ab}
+        for pname, fn in (("fused", fused), ("split", split)):
+            for _ in range(5):
+                fn()
+            cold = med(_device_times(stream, fn, n, flush))
+            warm = med(_device_times(stream, fn, n))
+            rec[pname] = {"us_cold_l2": 1e3 * cold, "us_warm_l2": 1e3 * warm,
+                          "tokens_per_s_cold_l2": w.ntok / (cold / 1e3)}
+        out[key] = rec
+    for key, w in (("2_prompt_short", wl.PROMPT_SHORT), ("3_prompt_long", wl.PROMPT_LONG)):
+        fused, _, ab, valid = attn_case(w)
+        for _ in range(3):
+            fused()
+        t = _device_times(stream, fused, n, flush)
+        ms = sum(t) / len(t)
+        out[key] = {"workload": w.name, "us": 1e3 * ms, "tokens_per_s": w.ntok / (ms / 1e3), "valid_cells": valid,
+                    "algorithmic_bytes": ab, "logical_gbs": ab / (ms / 1e3) / 1e9,
+                    "frac_of_hbm_peak": ab / (ms / 1e3) / 1e9 / hbm}
+    sweep = []
+    T = wl.SCORE_NTOK
+    for pos0 in wl.SCORE_POS0:
+        C = pos0 + T
+        cache = wl.make_cache(C, seed=5)
+        kq, ksc = to(cache.kq), to(cache.ksc)
+        q = to(wl.queries_f32(T, seed=5))
+        sc = torch.empty((T, C), dtype=torch.float32, device=dev)
+        ws = torch.empty(qsa_score_workspace_bytes(T), dtype=torch.uint8, device=dev)
+        fn = lambda: qsa_score(q, kq, ksc, pos0, sc, ws)
+        for _ in range(3):
+            fn()
+        t = _device_times(stream, fn, n, flush)
+        ms = sum(t) / len(t)
+        pairs = score_pairs(T, pos0)
+        # bytes: the fp32 queries read by the head-sum pass and its hi/lo rows
+        # written, then the score kernel's own bytes
+        nb = T * HQ * D * 4 + (-(-T // 64) * 64) * 2 * D * 2 + score_bytes(T, pos0, C)
+        ex = score_flops_executed(T, pos0)
+        sweep.append({"pos0": pos0, "cells": C, "pairs": pairs, "us": 1e3 * ms, "tokens_per_s": T / (ms / 1e3),
+                      "algorithmic_bytes": nb, "gbs": nb / (ms / 1e3) / 1e9,
+                      "frac_of_hbm_peak": nb / (ms / 1e3) / 1e9 / hbm,
+                      "tensor_tflops_executed": ex / (ms / 1e3) / 1e12,
+                      "frac_of_f16_peak_executed": ex / (ms / 1e3) / 1e12 / tc,
+                      "tflops_head_summed_method": 2 * D * pairs / (ms / 1e3) / 1e12})
+        del sc
+    out["4_score_sweep"] = sweep
+    return out
 
 
 def run_pages(args, rank, world, local_rank):
@@ -652,12 +819,29 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        cb = cpu_baseline(args.cpu_sample_seconds)
-        line = {"impl": "reference", "metric": METRIC, "value": cb["value"] * 1.0, "unit": UNIT, "n_gpus": 0,
-                "steps": 1, "warmup": 0, "ms_per_step": 1e3 * args.ntok / cb["value"], "higher_is_better": True,
+        # The oracle on every host core; each step is a bounded sample of the
+        # workload's token rows, sized so that the whole run takes about two
+        # and a half minutes at most.
+        pool = OraclePool(os.cpu_count() or 1)
+        try:
+            n, dt = pool.run(pool.rows(pool.cores), pool.cores)
+            budget = min(5.0, 150.0 / max(1, args.steps + args.warmup))
+            nrows = int(max(pool.cores, min(NTOK, budget * n / dt)))
+            for w in range(args.warmup):
+                pool.run(pool.rows(nrows, offset=w), pool.cores)
+            walls = [pool.run(pool.rows(nrows, offset=args.warmup + k), pool.cores)[1] for k in range(args.steps)]
+        finally:
+            pool.close()
+        ms = 1e3 * sum(walls) / len(walls)
+        value = nrows / (ms / 1e3)
+        config["sample"] = (f"each step: {nrows} of the {NTOK} token rows, evenly spaced (offset by the step), "
+                            f"on {pool.cores} single-threaded oracle processes")
+        cb = {"value": value, "unit": UNIT, "cores": pool.cores, "kind": "oracle", "sample": config["sample"]}
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
                 "cpu_baseline": cb,
-                "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+                "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
 
@@ -713,6 +897,10 @@ def main():
             print(json.dumps(line), flush=True)
         return
     res = run_ours(args, rank, world, local_rank)
+    cfg = None
+    if not args.no_configs and args.ntok == NTOK and args.pos0 == POS0:
+        import torch
+        cfg = run_configs(torch.device("cuda", local_rank), max(20, min(args.steps, 200)))
     if rank != 0:
         return
     cb = None
@@ -725,7 +913,7 @@ def main():
                          "fp32 prep and scores; fp16 attention output",
             "data": "synthetic", "config": config, "roofline": res["roofline"], "cpu_baseline": cb,
             "e2e": res["e2e"], "clocks": res["clocks"], "gpu_launches": res["launches_per_step"] * args.steps,
-            "kernels": res["kernels"]}
+            "kernels": res["kernels"], "configs": cfg}
     print(json.dumps(line), flush=True)
 
 

@@ -219,7 +219,9 @@ typedef struct {
  *  - It never allocates: no cudaMalloc, cudaFree or allocating library call.
  *  - The first call on each device looks up the scratch array's device
  *    address (cudaGetSymbolAddress) with that device current; make that
- *    first call before any stream capture.
+ *    first call before any stream capture.  The address is kept for the
+ *    life of the process: it does not survive cudaDeviceReset(), after
+ *    which this entry point must not be called on that device again.
  *  - All calls share the one array and it keeps the last call's contents.
  *    Every call rewrites what it reads, so nothing needs clearing, but two
  *    calls whose kernels overlap on the GPU (different streams without an
@@ -262,6 +264,27 @@ typedef struct {
 } qsa_select_args;
 
 qsa_status qsa_select(const qsa_select_args *args, void *stream);
+
+/*
+ * qsa_fill_ids_decode, qsa_fill_ids_even -- the per-token selected-id lists of
+ * the two workload families, written on the device (ids [ntok, width] int32,
+ * a device pointer owned by the caller, 4-byte aligned; every element is
+ * written).  For token t at position p = pos0 + t:
+ *  decode ("round 5 track b: cached residual norms and fused mtp attention",
+ *  section "mtp attention": 64 sink + 256 previous local + the current
+ *  cell): the cells 0 .. min(sink, p)-1, then max(sink, p-local) .. p-1,
+ *  then p, ascending, then -1.  Requires sink + local + 1 <= width.
+ *  even ("round 11 track b: qsa attention and score", sections "boundaries
+ *  and provenance" and "implementation and evaluator": evenly spaced unique
+ *  causal cells, unused slots poisoned with -1): with n = p + 1 and
+ *  k = min(n, select), slot j < k holds j when k == n and
+ *  floor(j (n-1) / (k-1)) otherwise (so 0 and p are always present), then
+ *  -1.  Requires 2 <= select <= width.
+ * Both are integer closed forms, exact.  Arguments are checked before
+ * anything is enqueued (QSA_ERR_INVALID_ARG).
+ */
+qsa_status qsa_fill_ids_decode(int ntok, int pos0, int width, int sink, int local, int32_t *ids, void *stream);
+qsa_status qsa_fill_ids_even(int ntok, int pos0, int width, int select, int32_t *ids, void *stream);
 
 qsa_status qsa_prep(const qsa_prep_args *args, void *stream);
 qsa_status qsa_score(const qsa_score_args *args, void *stream);

@@ -9,6 +9,7 @@ are rejected rather than computed elsewhere.
     qsa_score  head-reduced fp32 scores of every causal cache cell
     qsa_select per-token selected cell ids from the scores
     qsa_attn   chunked attention over per-token selected cell ids
+    qsa_fill_ids_decode / qsa_fill_ids_even  the workloads' id lists, on the device
 """
 from __future__ import annotations
 
@@ -19,7 +20,8 @@ from . import _abi
 from ._abi import (QSA_DEVERR_BAD_ID, QSA_DEVERR_TIMEOUT, QSA_SCORE_NOALLOC_MAX_TOKENS,  # noqa: F401
                    QSA_SELECT_MAX_CELLS, QSAError, lib)
 
-__all__ = ["qsa_prep", "qsa_score", "qsa_score_noalloc", "qsa_select", "qsa_attn", "qsa_score_workspace_bytes", "qsa_abi_version",
+__all__ = ["qsa_prep", "qsa_score", "qsa_score_noalloc", "qsa_select", "qsa_attn", "qsa_score_workspace_bytes",
+           "qsa_fill_ids_decode", "qsa_fill_ids_even", "qsa_abi_version",
            "QSAError", "QSA_DEVERR_BAD_ID", "QSA_DEVERR_TIMEOUT", "QSA_SCORE_NOALLOC_MAX_TOKENS",
            "QSA_SELECT_MAX_CELLS", "lib"]
 
@@ -139,6 +141,24 @@ def qsa_select(scores, pos0, ids, budget=2048, sink=64, local=256, stream=None):
                         local=int(local), scores=_ptr(scores, "scores", torch.float32), ld=scores.shape[1],
                         ids=_ptr(ids, "ids", torch.int32))
     _abi.check(lib().qsa_select(ctypes.byref(a), _stream(stream)))
+
+
+def qsa_fill_ids_decode(ids, pos0, sink=64, local=256, stream=None):
+    """ids [T, W] int32 <- each token's decode window (sink cells, the
+    previous `local` cells, its own cell p = pos0 + t), ascending, -1 padded."""
+    import torch
+    T, W = ids.shape
+    _abi.check(lib().qsa_fill_ids_decode(T, int(pos0), W, int(sink), int(local),
+                                         _ptr(ids, "ids", torch.int32), _stream(stream)))
+
+
+def qsa_fill_ids_even(ids, pos0, select=2048, stream=None):
+    """ids [T, W] int32 <- up to `select` evenly spaced causal cells of each
+    token (always 0 and p = pos0 + t), ascending, -1 padded."""
+    import torch
+    T, W = ids.shape
+    _abi.check(lib().qsa_fill_ids_even(T, int(pos0), W, int(select), _ptr(ids, "ids", torch.int32),
+                                       _stream(stream)))
 
 
 def qsa_attn(q, kq, vq, ksc, vsc, ids, out, softmax_scale=None, part=None, err=None, gate=None, stream=None):

@@ -61,33 +61,57 @@ ABI_VERSION = 3  # the struct layouts above
 _lib = None
 
 
+def _load(path: str) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m sparse_selected_attention_gb300.build --all` "
+            "(the QSA path has no fallback)")
+    L = ctypes.CDLL(path)
+    _declare(L, path)
+    return L
+
+
+_variants = {}
+
+
+def variant(name: str) -> ctypes.CDLL:
+    """A test variant of the library (see build.VARIANTS), loaded beside the
+    release one with its own symbols; its functions take the same structs."""
+    if name not in _variants:
+        from .build import lib_path
+        _variants[name] = _load(lib_path(name))
+    return _variants[name]
+
+
 def lib() -> ctypes.CDLL:
     """The loaded libqsa.so; raises if it has not been built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(
-                f"{LIB_PATH} is missing: build it with `python -m sparse_selected_attention_gb300.build` "
-                "(the QSA path has no fallback)")
-        L = ctypes.CDLL(LIB_PATH)
-        for name, argt in (("qsa_prep", PrepArgs), ("qsa_score", ScoreArgs), ("qsa_attn", AttnArgs),
-                           ("qsa_score_noalloc", ScoreArgs), ("qsa_select", SelectArgs)):
-            f = getattr(L, name)
-            f.argtypes = [ctypes.POINTER(argt), _vp]
-            f.restype = _c_int
-        L.qsa_score_workspace_bytes.argtypes = [_c_int, _c_int]
-        L.qsa_score_workspace_bytes.restype = ctypes.c_size_t
-        L.qsa_status_str.argtypes = [_c_int]
-        L.qsa_status_str.restype = ctypes.c_char_p
-        L.qsa_last_error.argtypes = []
-        L.qsa_last_error.restype = ctypes.c_char_p
-        L.qsa_abi_version.argtypes = []
-        L.qsa_abi_version.restype = _c_int
-        if L.qsa_abi_version() != ABI_VERSION:
-            raise RuntimeError(f"{LIB_PATH} has ABI version {L.qsa_abi_version()}, these bindings expect "
-                               f"{ABI_VERSION}: rebuild it")
-        _lib = L
+        _lib = _load(LIB_PATH)
     return _lib
+
+
+def _declare(L: ctypes.CDLL, path: str) -> None:
+    for name, argt in (("qsa_prep", PrepArgs), ("qsa_score", ScoreArgs), ("qsa_attn", AttnArgs),
+                       ("qsa_score_noalloc", ScoreArgs), ("qsa_select", SelectArgs)):
+        f = getattr(L, name)
+        f.argtypes = [ctypes.POINTER(argt), _vp]
+        f.restype = _c_int
+    L.qsa_fill_ids_decode.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]
+    L.qsa_fill_ids_decode.restype = _c_int
+    L.qsa_fill_ids_even.argtypes = [_c_int, _c_int, _c_int, _c_int, _vp, _vp]
+    L.qsa_fill_ids_even.restype = _c_int
+    L.qsa_score_workspace_bytes.argtypes = [_c_int, _c_int]
+    L.qsa_score_workspace_bytes.restype = ctypes.c_size_t
+    L.qsa_status_str.argtypes = [_c_int]
+    L.qsa_status_str.restype = ctypes.c_char_p
+    L.qsa_last_error.argtypes = []
+    L.qsa_last_error.restype = ctypes.c_char_p
+    L.qsa_abi_version.argtypes = []
+    L.qsa_abi_version.restype = _c_int
+    if L.qsa_abi_version() != ABI_VERSION:
+        raise RuntimeError(f"{path} has ABI version {L.qsa_abi_version()}, these bindings expect "
+                           f"{ABI_VERSION}: rebuild it")
 
 
 def check(status: int) -> None:

@@ -3,7 +3,13 @@
 Each translation unit is compiled in parallel for exactly one target,
 sm_103a, then linked into a shared library next to this file.  The CUDA
 runtime is linked statically, so the library needs only the driver at run
-time.  Usage:  python -m sparse_selected_attention_gb300.build [-v]
+time.  Usage:  python -m sparse_selected_attention_gb300.build [-v] [--all]
+
+Besides the release library there are test variants of the same sources,
+built by build_all():
+  libqsa_wait0.so  every bounded pipeline wait gives up at once
+                   (QSA_WAIT_LIMIT=0), so a test can watch the time-out path
+                   set its error bit and stop cleanly.
 """
 from __future__ import annotations
 
@@ -19,7 +25,12 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqsa.so")
-SOURCES = ["api.cpp", "prep.cu", "score.cu", "select.cu", "attn.cu", "attn_tc.cu"]
+# variant -> (extra defines, library file)
+VARIANTS = {
+    "release": ([], "libqsa.so"),
+    "wait0": (["-DQSA_WAIT_LIMIT=0"], "libqsa_wait0.so"),
+}
+SOURCES = ["api.cpp", "prep.cu", "score.cu", "select.cu", "attn.cu", "ids.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 
@@ -49,9 +60,17 @@ def _stale(out: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) -> str:
-    """Compile and link; returns the library path.  Rebuilds only stale parts."""
-    os.makedirs(BUILD, exist_ok=True)
+def lib_path(variant: str = "release") -> str:
+    return os.path.join(PKG, VARIANTS[variant][1])
+
+
+def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False, variant: str = "release") -> str:
+    """Compile and link one variant; returns the library path.  Rebuilds only
+    stale parts."""
+    defines, libname = VARIANTS[variant]
+    bdir = BUILD if variant == "release" else os.path.join(BUILD, variant)
+    lib = os.path.join(PKG, libname)
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     headers = [os.path.join(INCLUDE, "qsa.h")] + [
         os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
@@ -59,23 +78,35 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
     objs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src + ".o")
+        o = os.path.join(bdir, src + ".o")
         objs.append(o)
         if force or _stale(o, [s] + headers):
             extra = ["-Xptxas", "-v"] if (ptxas_info and src.endswith(".cu")) else []
-            jobs.append([cc, *ARCH, *FLAGS, *extra, "-c", s, "-o", o])
+            jobs.append([cc, *ARCH, *FLAGS, *defines, *extra, "-c", s, "-o", o])
     with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
         results = list(ex.map(lambda c: _run(c, verbose), jobs))
     if ptxas_info:
         for r in results:
             sys.stdout.write(r.stderr)
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + ".tmp"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + ".tmp"
         _run([cc, *ARCH, "-shared", "-o", tmp, *objs], verbose)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
+
+
+def build_all(verbose: bool = False, force: bool = False) -> list:
+    """Every variant (release first), the variants in parallel."""
+    out = [build(verbose=verbose, force=force)]
+    rest = [v for v in VARIANTS if v != "release"]
+    with ThreadPoolExecutor(max_workers=len(rest)) as ex:
+        out += list(ex.map(lambda v: build(verbose=verbose, force=force, variant=v), rest))
+    return out
 
 
 if __name__ == "__main__":
     v = "-v" in sys.argv
-    print(build(verbose=v, ptxas_info="--ptxas" in sys.argv, force="--force" in sys.argv))
+    if "--all" in sys.argv:
+        print("\n".join(build_all(verbose=v, force="--force" in sys.argv)))
+    else:
+        print(build(verbose=v, ptxas_info="--ptxas" in sys.argv, force="--force" in sys.argv))

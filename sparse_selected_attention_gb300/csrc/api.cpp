@@ -177,6 +177,33 @@ qsa_status qsa_select(const qsa_select_args *a, void *stream) {
     return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_select");
 }
 
+qsa_status qsa_fill_ids_decode(int ntok, int pos0, int width, int sink, int local, int32_t *ids, void *stream) {
+    g_last_error[0] = 0;
+    if (ntok < 0 || pos0 < 0 || sink < 0 || local < 0)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_fill_ids_decode: negative ntok, pos0, sink or local");
+    if (width <= 0 || (long long)sink + local + 1 > width)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_fill_ids_decode: width must hold sink + local + 1 ids");
+    if ((long long)pos0 + ntok > 0x7fffffffll) return fail(QSA_ERR_INVALID_ARG, "qsa_fill_ids_decode: positions beyond int32");
+    if (ntok == 0) return QSA_OK;
+    if (!ids || !aligned(ids, 4)) return fail(QSA_ERR_INVALID_ARG, "qsa_fill_ids_decode: NULL or misaligned ids");
+    qsa::FillIdsLaunch L{ntok, pos0, width, sink, local, 0, ids};
+    cudaError_t e = qsa::launch_fill_ids(L, false, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_fill_ids_decode");
+}
+
+qsa_status qsa_fill_ids_even(int ntok, int pos0, int width, int select, int32_t *ids, void *stream) {
+    g_last_error[0] = 0;
+    if (ntok < 0 || pos0 < 0) return fail(QSA_ERR_INVALID_ARG, "qsa_fill_ids_even: negative ntok or pos0");
+    if (select < 2 || width <= 0 || select > width)
+        return fail(QSA_ERR_INVALID_ARG, "qsa_fill_ids_even: need 2 <= select <= width");
+    if ((long long)pos0 + ntok > 0x7fffffffll) return fail(QSA_ERR_INVALID_ARG, "qsa_fill_ids_even: positions beyond int32");
+    if (ntok == 0) return QSA_OK;
+    if (!ids || !aligned(ids, 4)) return fail(QSA_ERR_INVALID_ARG, "qsa_fill_ids_even: NULL or misaligned ids");
+    qsa::FillIdsLaunch L{ntok, pos0, width, 0, 0, select, ids};
+    cudaError_t e = qsa::launch_fill_ids(L, true, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_fill_ids_even");
+}
+
 // Allocation-free scoring: same checks as qsa_score minus the workspace, plus
 // the built-in scratch limit.
 qsa_status qsa_score_noalloc(const qsa_score_args *a, void *stream) {

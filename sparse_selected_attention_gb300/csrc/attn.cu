@@ -793,12 +793,6 @@ cudaError_t launch_attn(const AttnLaunch &a, cudaStream_t s) {
     if (a.ntok == 0) return cudaSuccess;
     const bool wide = a.head_dim == 2 * D;
     if (a.part) return wide ? launch_split<2>(a, s) : launch_split<1>(a, s);
-#ifndef QSA_ATTN_TC
-#define QSA_ATTN_TC 0
-#endif
-#if QSA_ATTN_TC
-    if (!wide && a.n_kv_heads == 1 && !a.gate) return launch_attn_tc(a, s);
-#endif
 #ifndef QSA_ATTN_NW
 #define QSA_ATTN_NW 4
 #endif

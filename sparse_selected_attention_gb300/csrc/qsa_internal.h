@@ -57,6 +57,13 @@ struct SelectLaunch {
     int32_t *ids;
 };
 
+struct FillIdsLaunch {
+    int ntok, pos0, width;
+    int sink, local;  // decode window
+    int select;       // even lists: cells per token (at most)
+    int32_t *ids;     // [ntok, width]
+};
+
 // Longest score row (cells) the selection kernel holds on chip.
 constexpr int kSelectMaxCells = 32768;
 
@@ -70,8 +77,7 @@ cudaError_t launch_score(const ScoreLaunch &a, cudaStream_t s);
 cudaError_t launch_score_noalloc(const ScoreLaunch &a, cudaStream_t s);
 cudaError_t launch_attn(const AttnLaunch &a, cudaStream_t s);
 cudaError_t launch_select(const SelectLaunch &a, cudaStream_t s);
-// Fused attention on tcgen05 (attn_tc.cu); same contract as the fused path of
-// launch_attn (part == NULL).
-cudaError_t launch_attn_tc(const AttnLaunch &a, cudaStream_t s);
+// Decode windows (even = false) or evenly spaced causal lists (even = true).
+cudaError_t launch_fill_ids(const FillIdsLaunch &a, bool even, cudaStream_t s);
 
 }  // namespace qsa

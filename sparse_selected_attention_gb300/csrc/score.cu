@@ -43,8 +43,9 @@
 //    cell and 64 token columns, so every store instruction writes 32
 //    consecutive cells of one score row (128 bytes).
 // Every mbarrier wait is bounded; on expiry the kernel records
-// QSA_DEVERR_TIMEOUT, all roles stop, tensor memory is freed and the kernel
-// returns.
+// QSA_DEVERR_TIMEOUT and all roles stop; the MMA thread then waits (bounded)
+// for the MMAs it has issued, and only then is tensor memory freed and the
+// kernel returns.
 #include <cuda_fp16.h>
 
 #include <mutex>
@@ -75,7 +76,7 @@ constexpr uint32_t PLANE = TN * D * 2;          // one fp16 qbar plane (hi or lo
 constexpr uint32_t KBLOCK = TN * 128;           // bytes of one 64-wide K block of a plane
 constexpr uint32_t B_PAIR = 2 * PLANE;          // qbar hi + lo of one token tile
 constexpr uint32_t OFF_BAR = 2 * B_PAIR;        // two token tiles in flight
-constexpr uint32_t OFF_FLAG = OFF_BAR + (2 * NA + 8) * 8;
+constexpr uint32_t OFF_FLAG = OFF_BAR + (2 * NA + 9) * 8;
 constexpr uint32_t SMEM_USED = OFF_FLAG + 16;
 // All 512 tensor-memory columns and more than half of the shared memory: one
 // CTA per SM.
@@ -205,7 +206,7 @@ __global__ void __maxnreg__(72) score_kernel(ScoreLaunch a) {
     uint8_t *gen = smem_raw + (base - raw);
     const uint32_t sB = base, bar = base + OFF_BAR;
     const uint32_t a_full = bar, a_empty = bar + 8 * NA, b_full = bar + 16 * NA, b_empty = b_full + 16,
-                   acc_full = b_empty + 16, acc_empty = acc_full + 16;
+                   acc_full = b_empty + 16, acc_empty = acc_full + 16, drain = acc_empty + 16;
     volatile int *abort = reinterpret_cast<volatile int *>(gen + OFF_FLAG);
     volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gen + OFF_FLAG + 8);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -221,6 +222,7 @@ __global__ void __maxnreg__(72) score_kernel(ScoreLaunch a) {
             mbar_init(acc_full + 8 * i, 1);
             mbar_init(acc_empty + 8 * i, NEPI * 32);
         }
+        mbar_init(drain, 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -328,6 +330,7 @@ __global__ void __maxnreg__(72) score_kernel(ScoreLaunch a) {
         if (lane == 0) {
             Walker w = w0;
             int nb = 0, cur_tt = -1, bs = 0;
+            bool issued = false;
             for (int k = 0; k < n; ++k) {
                 if (w.tt != cur_tt) {
                     bs = nb & 1;
@@ -351,12 +354,20 @@ __global__ void __maxnreg__(72) score_kernel(ScoreLaunch a) {
                     mma_f16_ts(dt, ah + 8 * ks, bl + koff, IDESC, 1u);
                     mma_f16_ts(dt, al + 8 * ks, bh + koff, IDESC, 1u);
                 }
+                issued = true;
                 mma_commit(a_empty + 8 * st);
                 mma_commit(acc_full + 8 * b);
                 Walker nx = w;
                 walk_next(a, nx);
                 if (k + 1 == n || nx.tt != w.tt) mma_commit(b_empty + 8 * bs);
                 w = nx;
+            }
+            // Whether the loop finished or another role gave up, every MMA this
+            // thread issued must be complete before the tensor memory it
+            // writes is freed: one more commit tracks all of them.
+            if (issued) {
+                mma_commit(drain);
+                if (!mbar_wait_bounded(drain, 0, DRAIN_LIMIT)) *abort = 1;
             }
         }
     } else if (warp < NEPI) {

@@ -9,7 +9,16 @@
 namespace qsa {
 namespace tc {
 
-constexpr long long WAIT_LIMIT = 1ll << 24;  // mbarrier polls before giving up
+// mbarrier polls before a wait gives up.  A build may lower it: with
+// QSA_WAIT_LIMIT=0 every pipeline wait gives up at once, which exercises the
+// time-out path (error bit, orderly stop, tensor memory freed).
+#ifndef QSA_WAIT_LIMIT
+#define QSA_WAIT_LIMIT (1ll << 24)
+#endif
+constexpr long long WAIT_LIMIT = QSA_WAIT_LIMIT;
+// Polls of the final drain of issued MMAs before tensor memory is freed; not
+// lowered with the pipeline limit, since MMAs already issued always finish.
+constexpr long long DRAIN_LIMIT = 1ll << 24;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -59,6 +68,13 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
         if ((i & 255) == 255 && *abort) return false;
     }
     *abort = 1;
+    return false;
+}
+
+// Bounded wait that ignores the abort flag (the drain of issued MMAs).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit) {
+    for (long long i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
 

@@ -176,3 +176,37 @@ def test_score_rejects_negative_max_ctas(L, fn):
                        workspace_holds_qbar=0, max_ctas=-1)
     s, msg = _status(L, fn, a)
     assert s == _abi.QSA_ERR_INVALID_ARG and "max_ctas" in msg
+
+
+@pytest.mark.parametrize("args", [
+    (4, 100, 320, 64, 256, FAKE),      # width below sink + local + 1
+    (4, -1, 384, 64, 256, FAKE),
+    (4, 100, 384, -1, 256, FAKE),
+    (4, 100, 384, 64, 256, None),
+    (4, 100, 384, 64, 256, FAKE + 2),
+])
+def test_fill_ids_decode_rejects(L, args):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("argument-rejection checks use fake device addresses: run them on a machine without a GPU")
+    assert L.qsa_fill_ids_decode(*args, None) == _abi.QSA_ERR_INVALID_ARG
+    assert L.qsa_last_error().decode().startswith("qsa_fill_ids_decode")
+
+
+@pytest.mark.parametrize("args", [
+    (4, 100, 2048, 1, FAKE),           # select below 2
+    (4, 100, 1024, 2048, FAKE),        # select above width
+    (4, -5, 2048, 2048, FAKE),
+    (4, 100, 2048, 2048, None),
+])
+def test_fill_ids_even_rejects(L, args):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("argument-rejection checks use fake device addresses: run them on a machine without a GPU")
+    assert L.qsa_fill_ids_even(*args, None) == _abi.QSA_ERR_INVALID_ARG
+    assert L.qsa_last_error().decode().startswith("qsa_fill_ids_even")
+
+
+def test_fill_ids_zero_tokens_is_a_no_op(L):
+    assert L.qsa_fill_ids_even(0, 0, 64, 64, None, None) == _abi.QSA_OK
+    assert L.qsa_fill_ids_decode(0, 0, 384, 64, 256, None, None) == _abi.QSA_OK

@@ -1,11 +1,11 @@
 """qsa_attn on the GPU against the CPU oracle, through the C ABI.
 
-Covers the four attention workloads at full size (the decode ones and the
-short prompt one on every token, the long prompt one on a seeded sample of
-token rows that includes every edge-mode row of the sample), the width-2051
-case with a three-cell last chunk, the decode width matrix, padding-only
-tokens, out-of-range ids, the split (per-chunk + merge) path with its chunk
-partials, and other head counts.
+Covers the four attention workloads at full size on every token row (the
+long prompt one in each edge mode: plain, signed-zero queries, near-
+cancelling dot products), the pages' prompt matrix of token counts and
+start positions, the width-2051 case with a three-cell last chunk, the
+decode width matrix, padding-only tokens, out-of-range ids, the split
+(per-chunk + merge) path with its chunk partials, and other head counts.
 """
 import math
 
@@ -62,14 +62,12 @@ def test_prompt_short_full(cuda_device):
     check(q, cache, w.make_ids(), what=w.name)
 
 
-def _sample_rows(T, n, seed):
-    rng = np.random.default_rng(seed)
-    rows = set(rng.choice(T, size=n, replace=False).tolist()) | {0, 1, 63, 64, T - 1}
-    return np.array(sorted(rows))
-
-
 @pytest.mark.parametrize("edge", [0, 1, 2])
-def test_prompt_long_sampled(cuda_device, edge):
+def test_prompt_long_all_rows(cuda_device, edge):
+    # Every one of the 1984 token rows, in each edge mode run separately
+    # ("round 32 qsa flash experiment", candidate confirmation: both edge
+    # modes at T = 1984, pos0 = 30000; "round 11 track b", implementation and
+    # evaluator: whole output buffers compared).
     w = wl.PROMPT_LONG
     cache = wl.make_cache(w.cells, seed=w.seed)
     q = wl.queries_f16(w.ntok, seed=w.seed)
@@ -77,8 +75,7 @@ def test_prompt_long_sampled(cuda_device, edge):
         q = wl.edge_signed_zero(q)
     elif edge == 2:
         q, cache = wl.edge_cancellation(q, cache, seed=w.seed)
-    rows = _sample_rows(w.ntok, 96, 100 + edge)
-    out, _, _, _ = check(q, cache, w.make_ids(), rows=rows, what=f"{w.name} edge {edge}")
+    out, _, _, _ = check(q, cache, w.make_ids(), what=f"{w.name} edge {edge}")
     if edge == 1:
         # q = +-0: every score is 0, so the output is the plain mean of the rows.
         t = 7 * 11
@@ -86,6 +83,22 @@ def test_prompt_long_sampled(cuda_device, edge):
         v = cache.vq.astype(np.float64) * np.repeat(cache.vsc.astype(np.float64), 32, axis=1)
         mean = v[ids[ids >= 0]].mean(axis=0)
         assert_f16_close(out[t], np.broadcast_to(mean, (12, 128)), "signed-zero mean")
+
+
+# The pages' prompt cases ("round 11 track b: qsa attention and score",
+# implementation and evaluator): token counts 96 .. 1984 at start positions
+# 0, 1984, 2050 and 30000, each with the evenly spaced causal id lists (up
+# to 2048 per token, -1 padded to W = 2048); every token row.  The two cases
+# the full-size tests above already cover are left out.
+PAGES_MATRIX = [(T, p) for T in (96, 512, 1024, 1984) for p in (0, 1984, 2050, 30000)
+                if (T, p) not in ((1984, 0), (1984, 30000))]
+
+
+@pytest.mark.parametrize("T,pos0", PAGES_MATRIX)
+def test_pages_prompt_matrix(cuda_device, T, pos0):
+    cache = wl.make_cache(pos0 + T, seed=5)
+    q = wl.queries_f16(T, seed=5)
+    check(q, cache, wl.even_ids(T, pos0), what=f"T={T} pos0={pos0}")
 
 
 def test_width_2051_three_cell_last_chunk(cuda_device):

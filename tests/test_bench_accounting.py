@@ -58,3 +58,17 @@ def test_prep_bytes_per_token():
     pad = -(-T // 64) * 64
     assert bench.prep_bytes(T) == T * per + pad * 2 * 128 * 2 + 128 * 4
     assert bench.prep_bytes(T) == pytest.approx(21.87e6, rel=1e-3)
+
+
+def test_score_tiles_and_executed_flops():
+    # pos0 = 0: token tile tt (tokens 128 tt .. 128 tt + 127) reaches cell
+    # 128 tt + 127, i.e. tt + 1 cell tiles; the last tile (tokens 1920..1983)
+    # reaches cell 1983, 16 cell tiles: 1 + 2 + ... + 15 + 16 = 136.
+    assert bench.score_tiles(T, 0) == 136
+    # pos0 = 30000: tile tt's last token sits at 30000 + 128 tt + 127, so
+    # (30127 + 128 tt) // 128 + 1 = 235 + tt + 1 cell tiles for tt < 15
+    # (30127 = 235 * 128 + 47) and (30000 + 1983) // 128 + 1 = 250 for the
+    # last: 15 * 236 + (0 + 1 + ... + 14) + 250.
+    assert bench.score_tiles(T, 30000) == 15 * 236 + 105 + 250 == 3895
+    # three 128 x 128 x 128 fp16 products per tile, 2 flops per multiply-add
+    assert bench.score_flops_executed(T, 30000) == 3895 * 3 * 2 * 128 ** 3

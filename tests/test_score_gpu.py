@@ -1,9 +1,10 @@
 """qsa_score on the GPU against the CPU oracle, through the C ABI.
 
-Small shapes are compared on every causal cell; the four full-size positions
-(T = 1984 at pos0 0 / 2048 / 8192 / 30000) on a seeded sample of token rows
-that includes tile boundaries.  Every non-causal element of the output must
-still hold the caller's sentinel bit pattern, over the whole buffer.
+Small shapes are compared on every causal cell; the full-size sweep (T =
+1984 at pos0 0 / 2048 / 8192 / 30000, plus the pages' 2050 and 2052) on 128
+seeded token rows each, plus the rows at every 128-token tile boundary.
+Every non-causal element of the output must still hold the caller's sentinel
+bit pattern, over the whole buffer.
 """
 import numpy as np
 import pytest
@@ -65,15 +66,32 @@ def test_small_all_cells(cuda_device, T, pos0, dtype, row_align):
         assert torch.all(scores[rows, dead] == 0)
 
 
-@pytest.mark.parametrize("pos0", wl.SCORE_POS0)
+@pytest.mark.parametrize("pos0", sorted(set(wl.SCORE_POS0) | {1984, 2050, 2052}))
 def test_full_size_sampled_rows(cuda_device, pos0):
+    # The sweep's positions ("Round 36 Track C", 2. qsa_score_mm Loop
+    # Unrolling: pos0 0 / 2048 / 8192 / 30000) and the pages' others
+    # ("round 11 track b", score: valid negative result: 1984, 2050, 2052).
     T = wl.SCORE_NTOK
     cache = wl.make_cache(pos0 + T, seed=5)
     q = wl.queries_f32(T, seed=5)
     scores = run_gpu(q, cache, pos0)
     rng = np.random.default_rng(pos0)
-    rows = np.array(sorted(set(rng.choice(T, 24, replace=False).tolist()) | {0, 63, 64, 127, 1983}))
+    edges = {e for k in range(0, T + 1, 128) for e in (k - 1, k) if 0 <= e < T}
+    rows = np.array(sorted(set(rng.choice(T, 128, replace=False).tolist()) | edges))
     _compare(q, cache, pos0, scores, rows, f"T=1984 pos0={pos0}")
+
+
+# The rest of the pages' score matrix ("round 11 track b: qsa attention and
+# score", score: valid negative result: T = 96 / 512 / 1024 / 1984 at pos0 =
+# 0 / 1984 / 2050 / 2052 / 30000); T = 1984 is above.  Every causal cell of
+# every row.
+@pytest.mark.parametrize("T", [96, 512, 1024])
+@pytest.mark.parametrize("pos0", [0, 1984, 2050, 2052, 30000])
+def test_pages_score_matrix(cuda_device, T, pos0):
+    cache = wl.make_cache(pos0 + T, seed=5)
+    q = wl.queries_f32(T, seed=5)
+    scores = run_gpu(q, cache, pos0)
+    _compare(q, cache, pos0, scores, np.arange(T), f"T={T} pos0={pos0}")
 
 
 @pytest.mark.parametrize("cap", [1, 3, 7, 40])
