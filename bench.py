@@ -553,9 +553,14 @@ def bf16_peak():
 
 def _device_times(stream, fn, n, flush=None):
     """Device time of each of n calls of fn on `stream` (ms), L2 flushed
-    before each call when `flush` is given (outside the call's events)."""
+    before each call when `flush` is given (outside the call's events).
+    Without a flush the calls run back to back: a GPU-side sleep queued
+    first lets the host enqueue every call before the first one starts, so
+    no host launch gap falls between a call's events."""
     import torch
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    if flush is None:
+        torch.cuda._sleep(int(2e9 * 50e-6 * n))  # about 50 us of GPU time per call queued behind it
     for a, b in evs:
         if flush is not None:
             flush.zero_()

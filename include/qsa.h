@@ -75,10 +75,11 @@ typedef enum { QSA_F32 = 0, QSA_F16 = 1 } qsa_dtype;
  * qbar_out: NULL, or a qsa_score workspace for these ntok tokens (at least
  * qsa_score_workspace_bytes(ntok, head_dim) bytes, 256-byte aligned) that
  * receives the score's head sum of the rotated queries: per token, fp32
- * qbar[d] = sum_h q_out_f32[t,h,d] in head order, stored as the fp16 pair
- * hi = fp16(qbar), lo = fp16(qbar - hi), padding rows zero.  A following
- * qsa_score with workspace_holds_qbar = 1 then needs neither q nor its own
- * head-sum pass.
+ * qbar[d] = sum_h q_out_f32[t,h,d] in head order, scaled by the token's power
+ * of two 2^e (see qsa_score) and stored as the fp16 pair hi = fp16(qbar 2^e),
+ * lo = fp16(qbar 2^e - hi), with e after the rows; padding rows zero.  A
+ * following qsa_score with workspace_holds_qbar = 1 then needs neither q nor
+ * its own head-sum pass.
  *
  * Layouts (row-major, contiguous): q_in [ntok, n_q_heads, head_dim] fp32;
  * k_in, v_in [ntok, n_kv_heads, head_dim] fp32; norm_w [head_dim] fp32;
@@ -124,13 +125,16 @@ typedef struct {
  * tensor memory); n > 0 runs at most n.  A caller that overlaps the score with
  * other kernels on another stream caps it so that those kernels keep the
  * remaining SMs; the scores do not depend on the cap.  Negative is rejected.
- * Range: the head sum travels as an unscaled fp16 pair hi + lo.  Each
- * |qbar[t,d]| must stay below 65504 (beyond, it overflows to inf), and an
- * element's representation error is at most 2^-22 of it or 2^-25 absolute,
- * whichever is larger.  So the scores meet 1e-4 * sum|terms| for query values
- * of about 1e-3 and up -- every row out of qsa_prep with norm weights of
- * order one, whose head sums stay below a few hundred -- and lose relative
- * accuracy for rows of much smaller values.
+ * Range: the head sum qbar[t,:] = sum_h q[t,h,:] travels as an fp16 pair
+ * hi + lo under a per-token power of two 2^e_t: e_t = 0 while the row's
+ * largest |qbar| lies in [2^-4, 2^14), otherwise the row is scaled into
+ * [2^13, 2^14) (|e_t| <= 120), and the scores are multiplied back by 2^-e_t.
+ * Each element then carries about 22 significant bits relative to its row's
+ * largest, for any finite row whose largest element is between about 2^-107
+ * and the fp32 maximum; the scores meet 1e-4 * sum|terms| across that range.
+ * Elements more than about 2^37 below their row's largest keep less (the fp16
+ * lo part underflows), and a row with an inf or NaN gives non-finite scores,
+ * as the definition does.
  * Requires pos0 + ntok <= cache_cells.  Supported: head_dim == 128,
  * group == 32, 1 <= n_q_heads <= 64.  q, kq 16-byte aligned; ksc 8-byte.
  */
@@ -209,8 +213,8 @@ typedef struct {
  * not call cudaMalloc because that call can synchronise the device and has no
  * latency bound.  It computes exactly what qsa_score computes, but instead of
  * the caller's workspace it uses a scratch array built into the library
- * (QSA_SCORE_NOALLOC_MAX_TOKENS * 512 bytes = 4 MiB of device memory, held on
- * every GPU that loads the library until the process exits).  The
+ * (QSA_SCORE_NOALLOC_MAX_TOKENS * 516 bytes, about 4 MiB of device memory,
+ * held on every GPU that loads the library until the process exits).  The
  * `workspace`, `workspace_bytes` and `workspace_holds_qbar` fields are ignored:
  * the head sum is always computed from q; `max_ctas` applies as in qsa_score.
  *

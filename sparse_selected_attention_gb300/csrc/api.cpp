@@ -51,7 +51,7 @@ const char *qsa_status_str(qsa_status s) {
 size_t qsa_score_workspace_bytes(int ntok, int head_dim) {
     if (ntok < 0 || head_dim != kHeadDim) return 0;
     const size_t pad = ((size_t)ntok + qsa::kScoreTokTile - 1) / qsa::kScoreTokTile * qsa::kScoreTokTile;
-    return pad * 2 * (size_t)head_dim * sizeof(uint16_t);
+    return pad * qsa::kScoreWsBytesPerTok;
 }
 
 qsa_status qsa_prep(const qsa_prep_args *a, void *stream) {
@@ -87,6 +87,9 @@ qsa_status qsa_prep(const qsa_prep_args *a, void *stream) {
     L.rope_k = a->rope_k;
     L.qbar = static_cast<uint16_t *>(a->qbar_out);
     L.ntok_pad = (a->ntok + 63) / 64 * 64;
+    L.qexp = a->qbar_out ? reinterpret_cast<int *>(static_cast<uint8_t *>(a->qbar_out) +
+                                                   (size_t)L.ntok_pad * qsa::kScoreRowBytes)
+                         : nullptr;
     L.q_in = a->q_in;
     L.k_in = a->k_in;
     L.v_in = a->v_in;
@@ -123,8 +126,10 @@ qsa_status qsa_score(const qsa_score_args *a, void *stream) {
     if ((need_q && !aligned(a->q, 16)) || !aligned(a->kq, 16) || !aligned(a->ksc, 8) || !aligned(a->scores, 4) ||
         !aligned(a->workspace, 256))
         return fail(QSA_ERR_INVALID_ARG, "qsa_score: misaligned buffer");
+    const size_t pad = (size_t)(a->ntok + qsa::kScoreTokTile - 1) / qsa::kScoreTokTile * qsa::kScoreTokTile;
     qsa::ScoreLaunch L{a->ntok,   a->pos0, a->n_q_heads, a->cache_cells, a->q, a->q_dtype == QSA_F16 ? 1 : 0,
                        a->kq,     a->ksc,  a->scores,    a->ld,          static_cast<uint16_t *>(a->workspace),
+                       reinterpret_cast<int *>(static_cast<uint8_t *>(a->workspace) + pad * qsa::kScoreRowBytes),
                        a->err,    a->workspace_holds_qbar, a->max_ctas};
     cudaError_t e = qsa::launch_score(L, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_score");
@@ -228,7 +233,7 @@ qsa_status qsa_score_noalloc(const qsa_score_args *a, void *stream) {
     if (!aligned(a->q, 16) || !aligned(a->kq, 16) || !aligned(a->ksc, 8) || !aligned(a->scores, 4))
         return fail(QSA_ERR_INVALID_ARG, "qsa_score_noalloc: misaligned buffer");
     qsa::ScoreLaunch L{a->ntok, a->pos0, a->n_q_heads, a->cache_cells, a->q, a->q_dtype == QSA_F16 ? 1 : 0,
-                       a->kq,   a->ksc,  a->scores,    a->ld,          nullptr, a->err,
+                       a->kq,   a->ksc,  a->scores,    a->ld,          nullptr, nullptr, a->err,
                        0,       a->max_ctas};
     cudaError_t e = qsa::launch_score_noalloc(L, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_score_noalloc");

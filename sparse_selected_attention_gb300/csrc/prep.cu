@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(384, 4) prep_kernel(PrepParams P) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (t >= a.ntok) {  // padding rows of the score's head sum
         for (int i = threadIdx.x; i < 2 * D; i += blockDim.x) a.qbar[(size_t)t * 2 * D + i] = 0;
+        if (threadIdx.x == 0) a.qexp[t] = 0;
         return;
     }
     __shared__ float4 qrows[MAXQH][D / 4];  // rotated query rows, for the head sum
@@ -198,17 +199,43 @@ __global__ void __launch_bounds__(384, 4) prep_kernel(PrepParams P) {
     }
     if (a.qbar) {
         // The score's head sum: fp32, heads in order (as the score's own
-        // head-sum pass adds the fp32 rows), split into an fp16 hi/lo pair.
+        // head-sum pass adds the fp32 rows), scaled by the token's power of
+        // two and split into an fp16 hi/lo pair.  A block has at least 96
+        // threads, so each thread sums at most two of the 128 dims.
+        __shared__ float wmax[12];
         __syncthreads();
-        for (int d = threadIdx.x; d < D; d += blockDim.x) {
-            const float *rows = reinterpret_cast<const float *>(qrows);
-            float sum = 0.0f;
-            for (int h = 0; h < a.n_q_heads; ++h) sum += rows[h * D + d];
-            const __half hi = __float2half_rn(sum);
-            const __half lo = __float2half_rn(sum - __half2float(hi));
-            a.qbar[(size_t)t * 2 * D + d] = __half_as_ushort(hi);
-            a.qbar[(size_t)t * 2 * D + D + d] = __half_as_ushort(lo);
+        const float *rows = reinterpret_cast<const float *>(qrows);
+        float sums[2] = {0.0f, 0.0f}, m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int d = threadIdx.x + i * blockDim.x;
+            if (d < D) {
+                float sum = 0.0f;
+                for (int h = 0; h < a.n_q_heads; ++h) sum += rows[h * D + d];
+                sums[i] = sum;
+                m = fmaxf(m, fabsf(sum));
+            }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) wmax[warp] = m;
+        __syncthreads();
+        m = wmax[0];
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, wmax[w]);
+        const int e = head_sum_exponent(m);
+        const float f = exp2i(e);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int d = threadIdx.x + i * blockDim.x;
+            if (d < D) {
+                const float v = sums[i] * f;
+                const __half hi = __float2half_rn(v);
+                const __half lo = __float2half_rn(v - __half2float(hi));
+                a.qbar[(size_t)t * 2 * D + d] = __half_as_ushort(hi);
+                a.qbar[(size_t)t * 2 * D + D + d] = __half_as_ushort(lo);
+            }
+        }
+        if (threadIdx.x == 0) a.qexp[t] = e;
     }
 }
 

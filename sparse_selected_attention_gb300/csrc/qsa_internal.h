@@ -18,7 +18,8 @@ struct PrepLaunch {
     int8_t *kq, *vq;
     uint16_t *ksc, *vsc;
     int rope_k;  // rotate the key rows (same pairs and angles as the queries) before quantising
-    uint16_t *qbar;  // NULL or [ntok_pad, 2, 128] fp16: the score's head sum (hi row, lo row)
+    uint16_t *qbar;  // NULL or [ntok_pad, 2, 128] fp16: the score's scaled head sum (hi row, lo row)
+    int *qexp;       // [ntok_pad]: each token's power-of-two exponent of that scaling (with qbar)
     int ntok_pad;    // ntok rounded up to 64 (rows of qbar)
 };
 
@@ -30,7 +31,8 @@ struct ScoreLaunch {
     const uint16_t *ksc;
     float *scores;
     int64_t ld;
-    uint16_t *qsum;  // workspace: [ntok_pad, 2, 128] fp16 (hi row, lo row)
+    uint16_t *qsum;  // workspace: [ntok_pad, 2, 128] fp16 (hi row, lo row) of the scaled head sum,
+    int *qexp;       // then [ntok_pad] int32 exponents: head sum = (hi + lo) * 2^-qexp
     unsigned int *err;
     int qsum_ready;  // the workspace already holds the head sum (written by prep)
     int max_ctas;    // 0: one persistent CTA per SM; n > 0: at most n
@@ -69,6 +71,32 @@ constexpr int kSelectMaxCells = 32768;
 
 // Token rows of the score workspace are padded to this multiple.
 constexpr int kScoreTokTile = 64;
+// Workspace bytes per (padded) token: the fp16 hi and lo rows of 128 dims,
+// then one int32 exponent.
+constexpr int kScoreRowBytes = 2 * 128 * 2;
+constexpr int kScoreWsBytesPerTok = kScoreRowBytes + 4;
+
+#ifdef __CUDACC__
+// The head sum's per-token power of two.  m is the largest |qbar[t, d]| of
+// the token.  The fp16 hi/lo pair represents values in [2^-4, 2^14) to about
+// 2^-22 of the row's maximum, so such rows keep exponent 0 (no scaling, the
+// common case); other finite non-zero rows are scaled by 2^e so that m 2^e
+// lies in [2^13, 2^14), with e limited to [-120, 120] so that 2^-e stays a
+// normal float.  A zero, infinite or all-NaN row keeps 0.
+__device__ __forceinline__ int head_sum_exponent(float m) {
+    if (!(m > 0.0f) || m > 3.4028234663852886e38f) return 0;
+    if (m >= 0.0625f && m < 16384.0f) return 0;
+    int adj = 0;
+    if (m < 1e-30f) {  // bring subnormal maxima into the normal range first (exact)
+        m *= 18446744073709551616.0f;  // 2^64
+        adj = 64;
+    }
+    const int lg = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127 - adj;  // floor(log2 m)
+    const int e = 13 - lg;
+    return e < -120 ? -120 : (e > 120 ? 120 : e);
+}
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }  // |e| <= 126
+#endif
 
 cudaError_t launch_prep(const PrepLaunch &a, cudaStream_t s);
 cudaError_t launch_score(const ScoreLaunch &a, cudaStream_t s);

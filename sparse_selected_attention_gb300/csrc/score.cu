@@ -129,10 +129,22 @@ __global__ void __launch_bounds__(D) qsum_kernel(ScoreLaunch a) {
                 if (h0 + i < a.n_q_heads) s += v[i];
         }
     }
-    const __half hi = __float2half_rn(s);
-    const __half lo = __float2half_rn(s - __half2float(hi));
+    // The token's power of two (the same rule and order as qsa_prep's head
+    // sum, so both write the same workspace bit for bit).
+    __shared__ float wmax[D / 32];
+    float m = fabsf(s);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((d & 31) == 0) wmax[d >> 5] = m;
+    __syncthreads();
+    m = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+    const int e = head_sum_exponent(m);
+    const float v = s * exp2i(e);
+    const __half hi = __float2half_rn(v);
+    const __half lo = __float2half_rn(v - __half2float(hi));
     a.qsum[(size_t)t * 2 * D + d] = __half_as_ushort(hi);
     a.qsum[(size_t)t * 2 * D + D + d] = __half_as_ushort(lo);
+    if (d == 0) a.qexp[t] = e;
 }
 
 __device__ __forceinline__ int cell_tiles(const ScoreLaunch &a, int tt) {
@@ -378,6 +390,7 @@ __global__ void __maxnreg__(72) score_kernel(ScoreLaunch a) {
         // per-element tests.  For a fixed column the warp's 32
         // lanes store 32 consecutive cells of one score row.
         const int quarter = warp & 3, half = warp >> 2;
+        const int ntok_pad = (a.ntok + 63) / 64 * 64;  // rows of the workspace
         auto cell_scales = [&](const Walker &wk) {
             const int c = wk.ct * TM + quarter * 32 + lane;
             return c < a.cache_cells ? __ldg(reinterpret_cast<const uint2 *>(a.ksc + (size_t)c * 4))
@@ -399,6 +412,10 @@ __global__ void __maxnreg__(72) score_kernel(ScoreLaunch a) {
             const bool full = c0 + TM - 1 <= a.pos0 + t0 && t0 + TN <= a.ntok;
             const int tmin = cell - a.pos0;            // first token whose causal range reaches `cell`
             float *col = a.scores + (size_t)tw * a.ld + cell;
+            // The head-sum exponents of this warp's 64 token columns, two per
+            // lane (tokens past the workspace's rows are never stored).
+            const int te = tw + 2 * lane;
+            const int2 ex = te < ntok_pad ? __ldg(reinterpret_cast<const int2 *>(a.qexp + te)) : make_int2(0, 0);
             if (!mbar_wait_or_abort(acc_full + 8 * b, (k >> 1) & 1, abort)) break;
             fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * TN + half * (TN / 2));
@@ -410,10 +427,20 @@ __global__ void __maxnreg__(72) score_kernel(ScoreLaunch a) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) asm volatile("" : "+r"(va[j]), "+r"(vb[j]));
             };
+            // Tokens whose head sum was scaled (exponent != 0) need their own
+            // factor 2^-e_t; in the common case no token of the warp's 64 was.
+            const bool unit = __all_sync(0xffffffffu, (ex.x | ex.y) == 0);
             // Streaming stores: the scores are not read again by this pass.
             auto store16 = [&](const uint32_t (&v)[16], int j0) {
                 float *p = col + (size_t)j0 * a.ld;
-                if (full) {
+                if (!unit) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j, p += a.ld) {
+                        const int c = j0 + j, t = tw + c;
+                        const float f = exp2i(-__shfl_sync(0xffffffffu, (c & 1) ? ex.y : ex.x, c >> 1));
+                        if (full || (t < a.ntok && t >= tmin)) __stcs(p, fmaf(__uint_as_float(v[j]), inv, 0.0f) * f);
+                    }
+                } else if (full) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j, p += a.ld) __stcs(p, fmaf(__uint_as_float(v[j]), inv, 0.0f));
                 } else {
@@ -491,8 +518,10 @@ cudaError_t launch_score(const ScoreLaunch &a, cudaStream_t s) {
 // the array, so calls whose kernels overlap on the GPU race on it.
 namespace {
 
-constexpr size_t kNoAllocElems = (size_t)QSA_SCORE_NOALLOC_MAX_TOKENS * 2 * D;  // fp16 hi/lo rows
-static __device__ __align__(256) uint16_t g_noalloc_qsum[kNoAllocElems];
+// One workspace of QSA_SCORE_NOALLOC_MAX_TOKENS rows: fp16 hi/lo rows, then
+// the per-token exponents.
+constexpr size_t kNoAllocBytes = (size_t)QSA_SCORE_NOALLOC_MAX_TOKENS * kScoreWsBytesPerTok;
+static __device__ __align__(256) uint8_t g_noalloc_qsum[kNoAllocBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
@@ -518,7 +547,9 @@ cudaError_t launch_score_noalloc(const ScoreLaunch &a, cudaStream_t s) {
         scratch = g_noalloc_addr[dev];
     }
     ScoreLaunch b = a;
+    const size_t pad = (size_t)(a.ntok + kScoreTokTile - 1) / kScoreTokTile * kScoreTokTile;
     b.qsum = static_cast<uint16_t *>(scratch);
+    b.qexp = reinterpret_cast<int *>(static_cast<uint8_t *>(scratch) + pad * kScoreRowBytes);
     return launch_score(b, s);
 }
 

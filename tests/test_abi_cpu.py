@@ -24,9 +24,10 @@ def test_exports_every_header_function(L):
 
 
 def test_workspace_bytes(L):
-    assert L.qsa_score_workspace_bytes(1, 128) == 64 * 512
-    assert L.qsa_score_workspace_bytes(1984, 128) == 1984 * 512
-    assert L.qsa_score_workspace_bytes(1985, 128) == 2048 * 512
+    # per padded token: fp16 hi and lo rows of 128 dims, one int32 exponent
+    assert L.qsa_score_workspace_bytes(1, 128) == 64 * 516
+    assert L.qsa_score_workspace_bytes(1984, 128) == 1984 * 516
+    assert L.qsa_score_workspace_bytes(1985, 128) == 2048 * 516
     assert L.qsa_score_workspace_bytes(10, 64) == 0
 
 

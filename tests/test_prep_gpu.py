@@ -87,13 +87,20 @@ def test_prep_rope_k(cuda_device, T, pos0, rope_dims):
     run_case(T, pos0, rope_dims=rope_dims, rope_k=True, seed=47)
 
 
-@pytest.mark.parametrize("T,heads", [(150, 12), (64, 1), (1, 30)])
-def test_prep_head_sum_feeds_the_score(cuda_device, T, heads):
-    """qsa_prep's qbar_out is the score's own head sum bit for bit, and a
-    score from it equals the score from q_out_f32 bit for bit."""
+@pytest.mark.parametrize("T,heads,wscale", [(150, 12, 1.0), (64, 1, 1.0), (1, 30, 1.0), (150, 12, 1e-6),
+                                             (150, 12, 1e6), (70, 12, 1e-25)])
+def test_prep_head_sum_feeds_the_score(cuda_device, T, heads, wscale):
+    """qsa_prep's qbar_out is the score's own head sum bit for bit (its
+    per-token power of two included), a score from it equals the score from
+    q_out_f32 bit for bit, and both match the oracle's score of q_out_f32 --
+    also with norm weights scaled far up or down, which moves every head sum
+    out of the unscaled fp16 range."""
+    from oracle import score, score_abs_bound
     from sparse_selected_attention_gb300 import qsa_score, qsa_score_workspace_bytes
+    from tests.gpu_helpers import assert_score_close
     pos0 = 3000
     inp = wl.prep_inputs(T, seed=48, heads=heads)
+    inp.norm_w = (inp.norm_w.astype(np.float64) * wscale).astype(np.float32)
     cache = wl.make_cache(pos0 + T, seed=48)
     kq, vq, ksc, vsc = dev(cache.kq), dev(cache.vq), dev(cache.ksc), dev(cache.vsc)
     q16 = torch.empty((T, heads, 128), dtype=torch.float16, device="cuda")
@@ -110,3 +117,9 @@ def test_prep_head_sum_feeds_the_score(cuda_device, T, heads):
     torch.cuda.synchronize()
     assert torch.equal(ws_prep, ws_score)                    # padding rows included
     assert torch.equal(s_q.view(torch.int32), s_bar.view(torch.int32))
+    q32n = q32.cpu().numpy()
+    kqn, kscn = kq.cpu().numpy(), ksc.cpu().numpy()         # with the rows prep just wrote
+    rows = np.arange(T)
+    ref = score(q32n, kqn, kscn, pos0, rows=rows)
+    A = score_abs_bound(q32n, kqn, kscn, pos0, rows=rows)
+    assert_score_close(s_bar.cpu().numpy(), ref, A, f"score from prep's head sum, weights x{wscale:g}")

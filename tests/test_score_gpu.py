@@ -127,15 +127,29 @@ def test_mixed_group_scales(cuda_device, ratio):
     _compare(q, cache, pos0, scores, np.arange(T), f"group scale ratio {ratio:g}")
 
 
-@pytest.mark.parametrize("mag", [3e-3, 2e3])
-def test_query_magnitudes_in_range(cuda_device, mag):
-    # The head sum travels as an unscaled fp16 hi/lo pair.  Near both ends of
-    # its stated range -- query values of a few 1e-3 (the lo parts partly
-    # subnormal) and head sums up to about 3e4 (fp16 tops out at 65504) --
-    # the scores still meet the 1e-4 A bound.
+@pytest.mark.parametrize("mag", [1e-30, 1e-6, 1e-4, 3e-3, 1.0, 1e3, 1e6, 1e30])
+def test_query_magnitudes(cuda_device, mag):
+    # The head sum travels as an fp16 hi/lo pair under a per-token power of
+    # two, so the 1e-4 A bound holds for query rows of any finite magnitude:
+    # rows far below fp16's normal range and far above its maximum alike.
     T, pos0 = 70, 300
     cache = wl.make_cache(pos0 + T, seed=37)
-    q = (wl.queries_f32(T, seed=37) * np.float32(mag)).astype(np.float32)
+    q = (wl.queries_f32(T, seed=37).astype(np.float64) * mag).astype(np.float32)
     scores = run_gpu(q, cache, pos0)
     assert bool(torch.isfinite(scores[0, : pos0 + 1]).all())
     _compare(q, cache, pos0, scores, np.arange(T), f"query magnitude {mag:g}")
+
+
+def test_query_magnitudes_mixed_in_one_tile(cuda_device):
+    # Tokens of very different magnitudes side by side in every 128-token
+    # tile (each token has its own power of two), plus all-zero rows and rows
+    # at the edges of the unscaled range.
+    T, pos0 = 300, 700
+    cache = wl.make_cache(pos0 + T, seed=39)
+    mags = np.array([1.0, 1e4, 1e-4, 1e-30, 1e30, 0.0, 2e-2, 5e3, 3e-3, 1e-12, 7e9])
+    m = mags[np.arange(T) % len(mags)]
+    q = (wl.queries_f32(T, seed=39).astype(np.float64) * m[:, None, None]).astype(np.float32)
+    scores = run_gpu(q, cache, pos0)
+    zero_rows = np.nonzero(m == 0)[0]
+    assert bool(torch.all(scores[torch.as_tensor(zero_rows, device="cuda"), : pos0 + 1] == 0))
+    _compare(q, cache, pos0, scores, np.arange(T), "mixed magnitudes")
