@@ -223,6 +223,22 @@ struct QRegs {
     }
 };
 
+// Q fragments in shared memory in fragment order: k-step k's four registers
+// for lane l at 16 (32 k + l) bytes, so each k-step is one conflict-free
+// 16-byte load per lane.  The warps that work on the same dims of the same
+// token share one copy.
+struct QSmem {
+    const uint4 *base;  // this lane's k-step 0
+    __device__ __forceinline__ void get(int k, uint32_t (&f)[4]) const {
+        const uint4 v = base[32 * k];
+        f[0] = v.x;
+        f[1] = v.y;
+        f[2] = v.z;
+        f[3] = v.w;
+    }
+};
+constexpr int QFRAG_BYTES = 8 * 32 * 16;  // one copy of a token's Q fragments (128 dims)
+
 // One 32-cell unit (id slots slot0 .. slot0+31, lane's id already loaded)
 // folded into the warp's state.  sl2 = softmax_scale * log2(e).  Sets `bad`
 // if an id was < -1 or >= cache_cells.
@@ -546,7 +562,7 @@ __device__ __forceinline__ void compute_staged(const uint8_t *stp, unsigned vmas
 
 // Exchange slots for S == 2: per warp, two parities of 16 floats x 32 lanes.
 template <int NW, int S>
-constexpr int xch_bytes() {
+__host__ __device__ constexpr int xch_bytes() {
     return S == 2 ? NW * 2 * 16 * 32 * (int)sizeof(float) : 0;
 }
 
@@ -567,51 +583,72 @@ __global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(Att
     uint8_t *ring = smem8 + warp * NS * STAGE_BYTES;
     const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
     float *xch = reinterpret_cast<float *>(smem8 + NW * NS * STAGE_BYTES);
-    QRegs qsrc;
-    load_q<S>(a, t, geo, qsrc.qa, a.softmax_scale < 0.0f);
+    // One copy of the Q fragments per dim half, written by the first group.
+    uint4 *qfrag = reinterpret_cast<uint4 *>(smem8 + NW * NS * STAGE_BYTES + xch_bytes<NW, S>());
+    if (pw == 0) {
+        uint32_t qa[8][4];
+        load_q<S>(a, t, geo, qa, a.softmax_scale < 0.0f);
+        uint4 *dst = qfrag + half * (QFRAG_BYTES / 16) + lane;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dst[32 * k] = make_uint4(qa[k][0], qa[k][1], qa[k][2], qa[k][3]);
+    }
+    __syncthreads();
+    QSmem qsrc{qfrag + half * (QFRAG_BYTES / 16) + lane};
     State st;
     state_init(st);
     bool bad = false;
 
-    // My group's units are u_i = pw + i*NP, i = 0 .. n-1.
+    // My group's units are u_i = pw + i*NP, i = 0 .. n-1.  A unit's ids are
+    // loaded one whole unit before its copies are issued (a ring of NS + 1
+    // registers), so the load's latency hides behind a unit of compute; they
+    // are validated when the copies are issued.
     const int n = pw < nunits ? (nunits - pw + NP - 1) / NP : 0;
-    auto unit_id = [&](int i) -> int {
-        if (i >= n) return -1;
-        int id = __ldg(idrow + (pw + i * NP) * UNIT + lane);
+    auto raw_id = [&](int i) -> int { return i < n ? __ldg(idrow + (pw + i * NP) * UNIT + lane) : -1; };
+    auto check_id = [&](int id) -> int {
         bad |= (id < -1) || (id >= a.cache_cells);
         return (id >= 0 && id < a.cache_cells) ? id : -1;
     };
-    int nx = 0;   // exchanges so far: their parity picks the slot (skipped units exchange nothing)
-    int idq[NS];  // ids of units i .. i+NS-1 (ring of registers)
+    constexpr int NQ = NS + 1;
+    int idq[NQ];  // ids of units i .. i+NS (validated once issued)
 #pragma unroll
-    for (int k = 0; k < NS; ++k) idq[k] = unit_id(k);
+    for (int k = 0; k < NQ; ++k) idq[k] = raw_id(k);
 #pragma unroll
     for (int k = 0; k < NS - 1; ++k) {
+        idq[k] = check_id(idq[k]);
         if (__any_sync(0xffffffffu, idq[k] >= 0)) issue_unit<S>(a, idq[k], ring_s + k * STAGE_BYTES, geo);
         cp_commit();
     }
+    int nx = 0;   // exchanges so far: their parity picks the slot (skipped units exchange nothing)
     for (int i = 0; i < n; ++i) {
         const int sI = i % NS;
         const int sN = (i + NS - 1) % NS;
-        // ids of unit i are idq[i % NS] ... rotate: after use, refill with unit i+NS
+        const int qI = i % NQ, qN = (i + NS - 1) % NQ, qL = (i + NS) % NQ;
         int id_i = 0, id_n = 0;
 #pragma unroll
-        for (int k = 0; k < NS; ++k) {
-            if (k == sI) id_i = idq[k];
-            if (k == sN) id_n = idq[k];
+        for (int k = 0; k < NQ; ++k) {
+            if (k == qI) id_i = idq[k];
+            if (k == qN) id_n = idq[k];
         }
-        if (__any_sync(0xffffffffu, id_n >= 0) && i + NS - 1 < n)
-            issue_unit<S>(a, id_n, ring_s + sN * STAGE_BYTES, geo);
+        if (i + NS - 1 < n) {
+            id_n = check_id(id_n);
+            if (__any_sync(0xffffffffu, id_n >= 0)) issue_unit<S>(a, id_n, ring_s + sN * STAGE_BYTES, geo);
+#pragma unroll
+            for (int k = 0; k < NQ; ++k)
+                if (k == qN) idq[k] = id_n;
+        }
         cp_commit();
+        // Unit i + NS's ids, used when its copies are issued next iteration;
+        // kept in their own register until this unit is computed, so that
+        // nothing waits for the load before then.
+        const int nid = raw_id(i + NS);
         cp_wait<NS - 1>();
         __syncwarp();
         const unsigned vmask = __ballot_sync(0xffffffffu, id_i >= 0);  // the same in both warps of a group
         if (vmask) compute_staged<S>(ring + sI * STAGE_BYTES, vmask, qsrc, st, sl2, half, xch, nx++ & 1);
         __syncwarp();
-        const int nid = unit_id(i + NS);
 #pragma unroll
-        for (int k = 0; k < NS; ++k)
-            if (k == sI) idq[k] = nid;
+        for (int k = 0; k < NQ; ++k)
+            if (k == qL) idq[k] = nid;
     }
     cp_wait<0>();
     if (__any_sync(0xffffffffu, bad) && lane == 0 && a.err) atomicOr(a.err, QSA_DEVERR_BAD_ID);
@@ -765,7 +802,7 @@ __global__ void __launch_bounds__(D * S) attn_merge_kernel(AttnLaunch a) {
 
 template <int NW, int NS, int S>
 cudaError_t launch_staged(const AttnLaunch &a, cudaStream_t s) {
-    size_t smem = (size_t)NW * NS * STAGE_BYTES + xch_bytes<NW, S>();
+    size_t smem = (size_t)NW * NS * STAGE_BYTES + xch_bytes<NW, S>() + (size_t)S * QFRAG_BYTES;
     const size_t merge = (size_t)(NW / S) * (16 * D * S + 48) * sizeof(float);
     if (smem < merge) smem = merge;
     cudaError_t e = cudaFuncSetAttribute(attn_staged_kernel<NW, NS, S>,
