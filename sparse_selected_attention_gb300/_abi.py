@@ -10,7 +10,9 @@ import os
 import re
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libqsa.so")
+# QSA_LIB names another build of the same library (the sanitizer tests load
+# libqsa_asan.so this way); there is no fallback when it is missing.
+LIB_PATH = os.environ.get("QSA_LIB") or os.path.join(_HERE, "libqsa.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "qsa.h")
 
 QSA_OK, QSA_ERR_INVALID_ARG, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3

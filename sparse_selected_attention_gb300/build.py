@@ -95,6 +95,29 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False, 
     return lib
 
 
+def build_host_sanitized(verbose: bool = False) -> str:
+    """libqsa_asan.so: the release kernels with the host side (api.cpp, the
+    argument validation) compiled by g++ under AddressSanitizer and
+    UndefinedBehaviorSanitizer.  For the CPU tests only; load it with the
+    sanitizer runtimes preloaded (tests/test_sanitizers_cpu.py)."""
+    build(verbose=verbose)
+    bdir = os.path.join(BUILD, "asan")
+    os.makedirs(bdir, exist_ok=True)
+    cuda_home = os.path.dirname(os.path.dirname(os.path.realpath(nvcc())))
+    gxx = shutil.which("g++")
+    if not gxx:
+        raise RuntimeError("g++ not found")
+    san = ["-fsanitize=address,undefined", "-fno-omit-frame-pointer", "-fno-sanitize-recover=undefined"]
+    api_o = os.path.join(bdir, "api.cpp.o")
+    _run([gxx, "-O1", "-g", "-std=c++17", "-fPIC", *san, "-I", INCLUDE, "-I", CSRC,
+          "-I", os.path.join(cuda_home, "include"), "-c", os.path.join(CSRC, "api.cpp"), "-o", api_o], verbose)
+    objs = [os.path.join(BUILD, src + ".o") for src in SOURCES if src != "api.cpp"]
+    lib = os.path.join(PKG, "libqsa_asan.so")
+    _run([gxx, "-shared", *san, "-o", lib, api_o, *objs, "-L", os.path.join(cuda_home, "lib64"),
+          "-lcudart_static", "-ldl", "-lrt", "-lpthread"], verbose)
+    return lib
+
+
 def build_all(verbose: bool = False, force: bool = False) -> list:
     """Every variant (release first), the variants in parallel."""
     out = [build(verbose=verbose, force=force)]
