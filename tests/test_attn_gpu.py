@@ -192,3 +192,25 @@ def test_softmax_scales(cuda_device, scale, part):
     bound = 2e-3 + 1e-2 * np.abs(ref) + 2.0 ** -10 * mag
     worst = np.unravel_index(np.argmax(np.abs(g - ref) - bound), g.shape)
     assert np.all(np.abs(g - ref) <= bound), f"scale {scale}: worst at {worst}: gpu={g[worst]} ref={ref[worst]}"
+
+
+@pytest.mark.parametrize("part", [False, True])
+def test_large_scales_mix_fast_and_exact_units(cuda_device, part):
+    """The fused kernel forms operands as fp16((code + 128) * scale) with one
+    fused multiply-add and removes the offset with small correction products,
+    for units whose K scales stay below 16 and V scales below 64; other units
+    take the exact conversion.  Cells with scales far beyond both limits (K
+    values up to 127 * 40, V values up to 127 * 300) are scattered so that
+    rows mix both kinds of unit."""
+    cache = wl.make_cache(6000, seed=31)
+    ks = cache.ksc.astype(np.float32)
+    vs = cache.vsc.astype(np.float32)
+    ks[::37] = np.float32(40.0)
+    ks[5::101, 2] = np.float32(15.9)          # just inside the K limit
+    vs[::53] = np.float32(300.0)
+    vs[7::89, 1] = np.float32(63.9)           # just inside the V limit
+    cache.ksc[...] = ks.astype(np.float16)
+    cache.vsc[...] = vs.astype(np.float16)
+    q = (wl.queries_f16(30, seed=31).astype(np.float32) * np.float32(0.05)).astype(np.float16)
+    ids = wl.even_ids(30, 5970, width=1024, select=1000)
+    check(q, cache, ids, what=f"large scales (part={part})", part=part)
