@@ -99,11 +99,11 @@ def score_pairs(ntok, pos0):
 
 
 def score_bytes(ntok, pos0, cells):
-    """The head sum read (fp16 hi/lo rows, prep writes it), int8 codes + fp16
-    scales of every cell read, one fp32 score written per causal (token, cell)
-    pair."""
+    """The head sum read (fp16 hi/lo rows and one int32 exponent per token,
+    prep writes them), int8 codes + fp16 scales of every cell read, one fp32
+    score written per causal (token, cell) pair."""
     ntok_pad = -(-ntok // 64) * 64
-    return ntok_pad * 2 * D * 2 + cells * (D + 2 * (D // G)) + 4 * score_pairs(ntok, pos0)
+    return ntok_pad * (2 * D * 2 + 4) + cells * (D + 2 * (D // G)) + 4 * score_pairs(ntok, pos0)
 
 
 def select_bytes(ntok, pos0, sink=64, local=256):
@@ -116,9 +116,10 @@ def select_bytes(ntok, pos0, sink=64, local=256):
 
 def prep_bytes(ntok):
     """fp32 q, k, v rows read, fp16 q written, int8 K/V codes and fp16 scales
-    written, the score's head sum (fp16 hi/lo rows) written, the norm weight."""
+    written, the score's head sum (fp16 hi/lo rows and an int32 exponent per
+    token) written, the norm weight."""
     ntok_pad = -(-ntok // 64) * 64
-    return (ntok * HQ * D * (4 + 2) + 2 * ntok * D * 4 + 2 * ntok * (D + 2 * (D // G)) + ntok_pad * 2 * D * 2
+    return (ntok * HQ * D * (4 + 2) + 2 * ntok * D * 4 + 2 * ntok * (D + 2 * (D // G)) + ntok_pad * (2 * D * 2 + 4)
             + D * 4)
 
 
@@ -680,7 +681,7 @@ def run_configs(dev, n):
         pairs = score_pairs(T, pos0)
         # bytes: the fp32 queries read by the head-sum pass and its hi/lo rows
         # written, then the score kernel's own bytes
-        nb = T * HQ * D * 4 + (-(-T // 64) * 64) * 2 * D * 2 + score_bytes(T, pos0, C)
+        nb = T * HQ * D * 4 + (-(-T // 64) * 64) * (2 * D * 2 + 4) + score_bytes(T, pos0, C)
         ex = score_flops_executed(T, pos0)
         sweep.append({"pos0": pos0, "cells": C, "pairs": pairs, "us": 1e3 * ms, "tokens_per_s": T / (ms / 1e3),
                       "algorithmic_bytes": nb, "gbs": nb / (ms / 1e3) / 1e9,

@@ -56,7 +56,7 @@ def test_pages_shape_attention_bytes():
 def test_prep_bytes_per_token():
     per = 12 * 128 * (4 + 2) + 2 * 128 * 4 + 2 * (128 + 2 * 4)   # q in/out, k and v in, codes + scales out
     pad = -(-T // 64) * 64
-    assert bench.prep_bytes(T) == T * per + pad * 2 * 128 * 2 + 128 * 4
+    assert bench.prep_bytes(T) == T * per + pad * (2 * 128 * 2 + 4) + 128 * 4
     assert bench.prep_bytes(T) == pytest.approx(21.87e6, rel=1e-3)
 
 
@@ -72,3 +72,10 @@ def test_score_tiles_and_executed_flops():
     assert bench.score_tiles(T, 30000) == 15 * 236 + 105 + 250 == 3895
     # three 128 x 128 x 128 fp16 products per tile, 2 flops per multiply-add
     assert bench.score_flops_executed(T, 30000) == 3895 * 3 * 2 * 128 ** 3
+
+
+def test_score_bytes():
+    # head sum: 1984 padded tokens x (2 fp16 rows of 128 + one int32 exponent);
+    # cache: 31984 cells x (128 code bytes + 4 fp16 scales); scores: 4 B per
+    # causal pair (1984 * 30000 + 1 + 2 + ... + 1984 = 61,489,120 pairs)
+    assert bench.score_bytes(T, 30000, 31984) == 1984 * 516 + 31984 * 136 + 4 * 61_489_120 == 251_330_048
