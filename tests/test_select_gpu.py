@@ -32,14 +32,28 @@ def test_select_matches_oracle_random(cuda_device, T, pos0):
     assert np.array_equal(got, select_ids(sc, pos0))
 
 
-def test_select_full_size_sampled_rows(cuda_device):
+def test_select_full_size_all_rows(cuda_device):
     T, pos0 = 1984, 30000
     sc = wl.normal(71, 1, (T, pos0 + T)).astype(np.float32)
     got = run(sc, pos0)
-    rows = np.array([0, 1, 511, 512, 1000, 1983])
-    for t in rows:
-        want = select_ids(sc[t:t + 1], pos0 + t)[0]
-        assert np.array_equal(got[t], want), t
+    bad = [t for t in range(T) if not np.array_equal(got[t], select_ids(sc[t:t + 1], pos0 + t)[0])]
+    assert not bad, f"{len(bad)} rows differ, first {bad[:5]}"
+
+
+def test_select_sample_misses_the_threshold(cuda_device):
+    """Rows where every score inside 32 evenly spread runs of 32 cells is far
+    below all others: a selection that estimated its threshold from such a
+    sample would miss it.  Ids must equal the oracle's."""
+    T, pos0, sink, local = 6, 20000, 64, 256
+    sc = wl.normal(78, 1, (T, pos0 + T)).astype(np.float32)
+    for t in range(T):
+        p = pos0 + t
+        fs, fe = sink, p - local
+        nfree = fe - fs
+        for k in range(32):
+            start = fs + k * (nfree - 32) // 31
+            sc[t, start:start + 32] = -50.0 - k
+    assert np.array_equal(run(sc, pos0), select_ids(sc, pos0))
 
 
 def test_select_heavy_ties(cuda_device):
