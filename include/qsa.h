@@ -294,6 +294,18 @@ qsa_status qsa_prep(const qsa_prep_args *args, void *stream);
 qsa_status qsa_score(const qsa_score_args *args, void *stream);
 qsa_status qsa_attn(const qsa_attn_args *args, void *stream);
 
+/*
+ * qsa_check_word -- the pages have no counterpart to this call; it serves the
+ * device bounds-check build of the library.  Built with QSA_CHECK=1
+ * (libqsa_check.so), every kernel tests the index of its global-memory
+ * accesses against the size of its buffer as the call's arguments define
+ * it; an index outside sets bit 0 of a device word and that access is
+ * skipped (nothing traps).  This call ORs the words of every kernel file
+ * into *out (a host pointer) and clears them; it synchronises with the
+ * device.  The release build returns QSA_ERR_UNSUPPORTED and writes 0.
+ */
+qsa_status qsa_check_word(unsigned int *out);
+
 /* Static description of a status code. */
 const char *qsa_status_str(qsa_status s);
 /* Message of the last QSA_ERR_* returned on this host thread ("" if none). */

@@ -103,6 +103,8 @@ def _declare(L: ctypes.CDLL, path: str) -> None:
     L.qsa_fill_ids_decode.restype = _c_int
     L.qsa_fill_ids_even.argtypes = [_c_int, _c_int, _c_int, _c_int, _vp, _vp]
     L.qsa_fill_ids_even.restype = _c_int
+    L.qsa_check_word.argtypes = [_vp]
+    L.qsa_check_word.restype = _c_int
     L.qsa_score_workspace_bytes.argtypes = [_c_int, _c_int]
     L.qsa_score_workspace_bytes.restype = ctypes.c_size_t
     L.qsa_status_str.argtypes = [_c_int]

@@ -9,7 +9,10 @@ Besides the release library there are test variants of the same sources,
 built by build_all():
   libqsa_wait0.so  every bounded pipeline wait gives up at once
                    (QSA_WAIT_LIMIT=0), so a test can watch the time-out path
-                   set its error bit and stop cleanly.
+                   set its error bit and stop cleanly;
+  libqsa_check.so  device-side index checks (QSA_CHECK=1): an index outside
+                   its buffer sets a device word (read by qsa_check_word)
+                   and the access is skipped.
 """
 from __future__ import annotations
 
@@ -29,6 +32,7 @@ LIB = os.path.join(PKG, "libqsa.so")
 VARIANTS = {
     "release": ([], "libqsa.so"),
     "wait0": (["-DQSA_WAIT_LIMIT=0"], "libqsa_wait0.so"),
+    "check": (["-DQSA_CHECK=1"], "libqsa_check.so"),
 }
 SOURCES = ["api.cpp", "prep.cu", "score.cu", "select.cu", "attn.cu", "ids.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -85,6 +85,7 @@ qsa_status qsa_prep(const qsa_prep_args *a, void *stream) {
     L.eps = a->eps;
     L.rope_theta = a->rope_theta;
     L.rope_k = a->rope_k;
+    L.cache_cells = a->cache_cells;
     L.qbar = static_cast<uint16_t *>(a->qbar_out);
     L.ntok_pad = (a->ntok + 63) / 64 * 64;
     L.qexp = a->qbar_out ? reinterpret_cast<int *>(static_cast<uint8_t *>(a->qbar_out) +
@@ -207,6 +208,28 @@ qsa_status qsa_fill_ids_even(int ntok, int pos0, int width, int select, int32_t 
     qsa::FillIdsLaunch L{ntok, pos0, width, 0, 0, select, ids};
     cudaError_t e = qsa::launch_fill_ids(L, true, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QSA_OK : cuda_fail(e, "qsa_fill_ids_even");
+}
+
+qsa_status qsa_check_word(unsigned int *out) {
+    g_last_error[0] = 0;
+    if (!out) return fail(QSA_ERR_INVALID_ARG, "qsa_check_word: out is NULL");
+#if QSA_CHECK
+    unsigned int w = 0u;
+    cudaError_t (*const readers[])(unsigned int *) = {qsa::take_check_word_attn, qsa::take_check_word_score,
+                                                      qsa::take_check_word_prep, qsa::take_check_word_select,
+                                                      qsa::take_check_word_ids};
+    for (auto rd : readers) {
+        unsigned int v = 0u;
+        const cudaError_t e = rd(&v);
+        if (e != cudaSuccess) return cuda_fail(e, "qsa_check_word");
+        w |= v;
+    }
+    *out = w;
+    return QSA_OK;
+#else
+    *out = 0u;
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_check_word: this library was built without device index checks (QSA_CHECK)");
+#endif
 }
 
 // Allocation-free scoring: same checks as qsa_score minus the workspace, plus

@@ -40,6 +40,7 @@
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
+#include "check.cuh"
 #include "qsa.h"
 #include "qsa_internal.h"
 
@@ -188,9 +189,9 @@ __device__ __forceinline__ void load_q(const AttnLaunch &a, int t, const Geom &g
     for (int half = 0; half < 2; ++half) {
         const int h = g + 8 * half;
         uint32_t w[16];
-        if (h < geo.per) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                a.q + ((size_t)t * a.n_q_heads + geo.h0 + h) * (D * S) + D * geo.half + 32 * r);
+        const size_t qoff = ((size_t)t * a.n_q_heads + geo.h0 + h) * (D * S) + D * geo.half + 32 * r;
+        if (h < geo.per && QSA_IN(qoff + 31, (size_t)a.ntok * a.n_q_heads * D * S)) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.q + qoff);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint4 v = __ldg(src + i);
@@ -259,7 +260,8 @@ __device__ __forceinline__ void process_unit(const AttnLaunch &a, int id, const 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int c = __shfl_sync(0xffffffffu, id, 8 * j + g);
-        if (c >= 0) {
+        if (c >= 0 && QSA_IN(kv_row<S>(a, geo, c) + 32 * r + 31, (size_t)a.cache_cells * geo.kstride) &&
+            QSA_IN(scale_row(a, geo, c) + 3, (size_t)a.cache_cells * geo.sstride)) {
             const uint4 *src = reinterpret_cast<const uint4 *>(a.kq + kv_row<S>(a, geo, c) + 32 * r);
             kd[j][0] = __ldg(src);
             kd[j][1] = __ldg(src + 1);
@@ -276,7 +278,8 @@ __device__ __forceinline__ void process_unit(const AttnLaunch &a, int id, const 
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int c = __shfl_sync(0xffffffffu, id, 16 * kk + 2 * r + (e & 1) + 8 * (e >> 1));
-            if (c >= 0) {
+            if (c >= 0 && QSA_IN(kv_row<S>(a, geo, c) + 16 * g + 15, (size_t)a.cache_cells * geo.kstride) &&
+                QSA_IN(scale_row(a, geo, c) + 3, (size_t)a.cache_cells * geo.sstride)) {
                 vd[kk][e] = __ldg(reinterpret_cast<const uint4 *>(a.vq + kv_row<S>(a, geo, c) + 16 * g));
                 vs[kk][e] = __ushort_as_half(__ldg(a.vsc + scale_row(a, geo, c) + vgroup<S>(g, geo.half)));
             } else {
@@ -418,12 +421,12 @@ __device__ __forceinline__ void issue_unit(const AttnLaunch &a, int id, uint32_t
     for (int i = 0; i < 8; ++i) {
         const int cell = (lane >> 3) + 4 * i;
         const int c = __shfl_sync(0xffffffffu, id, cell);
-        const bool ok = c >= 0;
+        const bool ok = c >= 0 && QSA_IN(kv_row<S>(a, geo, c) + 16 * q + 15, (size_t)a.cache_cells * geo.kstride);
         const size_t off = kv_row<S>(a, geo, ok ? c : 0) + 16 * q;
         cp_async16(st + cell * D + ((q ^ (cell & 1)) << 4), a.kq + off, ok);
         cp_async16(st + UNIT * D + cell * D + ((q ^ (2 * ((cell >> 1) & 3))) << 4), a.vq + off, ok);
     }
-    const bool ok = id >= 0;
+    const bool ok = id >= 0 && QSA_IN(scale_row(a, geo, id) + 3, (size_t)a.cache_cells * geo.sstride);
     const size_t so = scale_row(a, geo, ok ? id : 0);
     cp_async8(st + 2 * UNIT * D + lane * 8, a.ksc + so, ok);
     cp_async8(st + 2 * UNIT * D + UNIT * 8 + lane * 8, a.vsc + so, ok);
@@ -603,7 +606,11 @@ __global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(Att
     // registers), so the load's latency hides behind a unit of compute; they
     // are validated when the copies are issued.
     const int n = pw < nunits ? (nunits - pw + NP - 1) / NP : 0;
-    auto raw_id = [&](int i) -> int { return i < n ? __ldg(idrow + (pw + i * NP) * UNIT + lane) : -1; };
+    auto raw_id = [&](int i) -> int {
+        return i < n && QSA_IN((size_t)t * a.width + (pw + i * NP) * UNIT + lane, (size_t)a.ntok * a.width)
+                   ? __ldg(idrow + (pw + i * NP) * UNIT + lane)
+                   : -1;
+    };
     auto check_id = [&](int id) -> int {
         bad |= (id < -1) || (id >= a.cache_cells);
         return (id >= 0 && id < a.cache_cells) ? id : -1;
@@ -722,6 +729,7 @@ __global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(Att
             r1 = fmaf(fw, o.y, r1);
         }
         const size_t oi = ((size_t)t * a.n_q_heads + geo.h0 + h) * DR + d;
+        if (!QSA_IN(oi + 1, (size_t)a.ntok * a.n_q_heads * DR)) continue;
         const __half2 hv = __floats2half2_rn(gated(a, oi, r0), gated(a, oi + 1, r1));
         *reinterpret_cast<__half2 *>(a.out + oi) = hv;
     }
@@ -749,7 +757,8 @@ __global__ void __launch_bounds__(NW * 32) attn_chunk_kernel(AttnLaunch a) {
     State st;
     state_init(st);
     bool bad = false;
-    const int id0 = __ldg(idrow + c * CHUNK + lane), id1 = __ldg(idrow + c * CHUNK + UNIT + lane);
+    const bool idok = QSA_IN((size_t)t * a.width + c * CHUNK + UNIT + lane, (size_t)a.ntok * a.width);
+    const int id0 = idok ? __ldg(idrow + c * CHUNK + lane) : -1, id1 = idok ? __ldg(idrow + c * CHUNK + UNIT + lane) : -1;
     process_unit<S>(a, id0, qsrc, st, sl2, bad, geo, xch, 0);
     process_unit<S>(a, id1, qsrc, st, sl2, bad, geo, xch, 1);
     if (__any_sync(0xffffffffu, bad) && lane == 0 && a.err) atomicOr(a.err, QSA_DEVERR_BAD_ID);
@@ -758,7 +767,9 @@ __global__ void __launch_bounds__(NW * 32) attn_chunk_kernel(AttnLaunch a) {
     for (int hf = 0; hf < 2; ++hf) {
         const int h = g + 8 * hf;
         if (h >= geo.per) continue;
-        float *dst = a.part + (((size_t)t * nch + c) * a.n_q_heads + geo.h0 + h) * (DR + 2);
+        const size_t pbase = (((size_t)t * nch + c) * a.n_q_heads + geo.h0 + h) * (DR + 2);
+        if (!QSA_IN(pbase + DR + 1, (size_t)a.ntok * nch * a.n_q_heads * (DR + 2))) continue;
+        float *dst = a.part + pbase;
 #pragma unroll
         for (int jd = 0; jd < 16; ++jd) {
             dst[D * half + 32 * r + jd] = st.o[jd][2 * hf];
@@ -779,6 +790,9 @@ __global__ void __launch_bounds__(D * S) attn_merge_kernel(AttnLaunch a) {
     const int t = blockIdx.x, d = threadIdx.x;
     const int nch = a.width / CHUNK;
     for (int h = 0; h < a.n_q_heads; ++h) {
+        if (!QSA_IN(((size_t)t * nch * a.n_q_heads + h) * (DR + 2) + (size_t)(nch - 1) * a.n_q_heads * (DR + 2) + DR + 1,
+                    (size_t)a.ntok * nch * a.n_q_heads * (DR + 2)))
+            continue;
         const float *base = a.part + ((size_t)t * nch * a.n_q_heads + h) * (DR + 2);
         const size_t cstride = (size_t)a.n_q_heads * (DR + 2);
         float M = -CUDART_INF_F;
@@ -796,7 +810,7 @@ __global__ void __launch_bounds__(D * S) attn_merge_kernel(AttnLaunch a) {
             res = O / L;
         }
         const size_t oi = ((size_t)t * a.n_q_heads + h) * DR + d;
-        a.out[oi] = __half_as_ushort(__float2half_rn(gated(a, oi, res)));
+        if (QSA_IN(oi, (size_t)a.ntok * a.n_q_heads * DR)) a.out[oi] = __half_as_ushort(__float2half_rn(gated(a, oi, res)));
     }
 }
 
@@ -837,3 +851,5 @@ cudaError_t launch_attn(const AttnLaunch &a, cudaStream_t s) {
 }
 
 }  // namespace qsa
+
+QSA_DEFINE_CHECK_READER(take_check_word_attn)

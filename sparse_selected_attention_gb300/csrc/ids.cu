@@ -12,6 +12,7 @@
 // all in integer arithmetic, so the lists are exact.
 #include <stdint.h>
 
+#include "check.cuh"
 #include "qsa_internal.h"
 
 namespace qsa {
@@ -33,7 +34,7 @@ __global__ void fill_decode_kernel(FillIdsLaunch a) {
         v = lo + (j - n1);
     else if (j == n1 + n2)
         v = p;
-    a.ids[i] = v;
+    if (QSA_IN(i, (long long)a.ntok * a.width)) a.ids[i] = v;
 }
 
 __global__ void fill_even_kernel(FillIdsLaunch a) {
@@ -44,7 +45,7 @@ __global__ void fill_even_kernel(FillIdsLaunch a) {
     const long long k = n < a.select ? n : a.select;
     int v = -1;
     if (j < k) v = (k == n) ? j : (int)(((long long)j * (n - 1)) / (k - 1));
-    a.ids[i] = v;
+    if (QSA_IN(i, (long long)a.ntok * a.width)) a.ids[i] = v;
 }
 
 }  // namespace
@@ -62,3 +63,6 @@ cudaError_t launch_fill_ids(const FillIdsLaunch &a, bool even, cudaStream_t s) {
 }
 
 }  // namespace qsa
+
+QSA_DEFINE_CHECK_READER(take_check_word_ids)
+

@@ -18,6 +18,7 @@
 
 #include <cmath>
 
+#include "check.cuh"
 #include "qsa_internal.h"
 
 namespace qsa {
@@ -51,6 +52,7 @@ __global__ void __launch_bounds__(384, 4) prep_kernel(PrepParams P) {
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (t >= a.ntok) {  // padding rows of the score's head sum
+        if (!QSA_IN(t, a.ntok_pad)) return;
         for (int i = threadIdx.x; i < 2 * D; i += blockDim.x) a.qbar[(size_t)t * 2 * D + i] = 0;
         if (threadIdx.x == 0) a.qexp[t] = 0;
         return;
@@ -72,7 +74,7 @@ __global__ void __launch_bounds__(384, 4) prep_kernel(PrepParams P) {
 #pragma unroll
         for (int j = 0; j < HPW; ++j) {
             const int h = HPW * warp + j;
-            if (h < a.n_q_heads)
+            if (h < a.n_q_heads && QSA_IN(((size_t)t * a.n_q_heads + h) * D + D - 1, (size_t)a.ntok * a.n_q_heads * D))
                 xs[j] = __ldg(reinterpret_cast<const float4 *>(a.q_in + ((size_t)t * a.n_q_heads + h) * D) + lane);
         }
     } else if (is_kv) {
@@ -142,6 +144,7 @@ __global__ void __launch_bounds__(384, 4) prep_kernel(PrepParams P) {
             const int h = HPW * warp + j;
             if (h >= a.n_q_heads) continue;
             const size_t row = ((size_t)t * a.n_q_heads + h) * D;
+            if (!QSA_IN(row + D - 1, (size_t)a.ntok * a.n_q_heads * D)) continue;
             if (a.qbar) qrows[h][lane] = make_float4(y[j][0], y[j][1], y[j][2], y[j][3]);
             const __half2 h01 = __floats2half2_rn(y[j][0], y[j][1]);
             const __half2 h23 = __floats2half2_rn(y[j][2], y[j][3]);
@@ -153,6 +156,7 @@ __global__ void __launch_bounds__(384, 4) prep_kernel(PrepParams P) {
                 reinterpret_cast<float4 *>(a.q_out_f32 + row)[lane] = make_float4(y[j][0], y[j][1], y[j][2], y[j][3]);
         }
     } else if (is_kv) {
+        if (!QSA_IN(a.pos0 + t, a.cache_cells)) return;
         int8_t *dst = (is_v ? a.vq : a.kq) + (size_t)(a.pos0 + t) * D;
         uint16_t *sdst = (is_v ? a.vsc : a.ksc) + (size_t)(a.pos0 + t) * (D / G);
         float xv[4] = {x.x, x.y, x.z, x.w};
@@ -223,6 +227,7 @@ __global__ void __launch_bounds__(384, 4) prep_kernel(PrepParams P) {
         m = wmax[0];
         for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, wmax[w]);
         const int e = head_sum_exponent(m);
+        if (!QSA_IN(t, a.ntok_pad)) return;
         const float f = exp2i(e);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -252,3 +257,6 @@ cudaError_t launch_prep(const PrepLaunch &a, cudaStream_t s) {
 }
 
 }  // namespace qsa
+
+QSA_DEFINE_CHECK_READER(take_check_word_prep)
+

@@ -21,6 +21,7 @@ struct PrepLaunch {
     uint16_t *qbar;  // NULL or [ntok_pad, 2, 128] fp16: the score's scaled head sum (hi row, lo row)
     int *qexp;       // [ntok_pad]: each token's power-of-two exponent of that scaling (with qbar)
     int ntok_pad;    // ntok rounded up to 64 (rows of qbar)
+    int cache_cells; // rows of kq, vq, ksc, vsc
 };
 
 struct ScoreLaunch {
@@ -107,5 +108,14 @@ cudaError_t launch_attn(const AttnLaunch &a, cudaStream_t s);
 cudaError_t launch_select(const SelectLaunch &a, cudaStream_t s);
 // Decode windows (even = false) or evenly spaced causal lists (even = true).
 cudaError_t launch_fill_ids(const FillIdsLaunch &a, bool even, cudaStream_t s);
+
+#if QSA_CHECK
+// The QSA_CHECK build's per-file check words (check.cuh), read and cleared.
+cudaError_t take_check_word_attn(unsigned int *out);
+cudaError_t take_check_word_score(unsigned int *out);
+cudaError_t take_check_word_prep(unsigned int *out);
+cudaError_t take_check_word_select(unsigned int *out);
+cudaError_t take_check_word_ids(unsigned int *out);
+#endif
 
 }  // namespace qsa

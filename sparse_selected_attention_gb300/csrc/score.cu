@@ -50,6 +50,7 @@
 
 #include <mutex>
 
+#include "check.cuh"
 #include "qsa.h"
 #include "qsa_internal.h"
 #include "tc_common.cuh"
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(D) qsum_kernel(ScoreLaunch a) {
             for (int i = 0; i < HB; ++i) {
                 const int h = h0 + i;
                 const size_t off = ((size_t)t * a.n_q_heads + h) * D + d;
-                v[i] = h >= a.n_q_heads ? 0.0f
+                v[i] = h >= a.n_q_heads || !QSA_IN(off, (size_t)a.ntok * a.n_q_heads * D) ? 0.0f
                        : F16          ? __half2float(__ldg(reinterpret_cast<const __half *>(a.q) + off))
                                       : __ldg(reinterpret_cast<const float *>(a.q) + off);
             }
@@ -142,6 +143,7 @@ __global__ void __launch_bounds__(D) qsum_kernel(ScoreLaunch a) {
     const float v = s * exp2i(e);
     const __half hi = __float2half_rn(v);
     const __half lo = __float2half_rn(v - __half2float(hi));
+    if (!QSA_IN(t, (a.ntok + 63) / 64 * 64)) return;
     a.qsum[(size_t)t * 2 * D + d] = __half_as_ushort(hi);
     a.qsum[(size_t)t * 2 * D + D + d] = __half_as_ushort(lo);
     if (d == 0) a.qexp[t] = e;
@@ -276,7 +278,7 @@ __global__ void __maxnreg__(72) score_kernel(ScoreLaunch a) {
         uint2 psc;
         auto load_a = [&](int ct) {
             const int c = ct * TM + row;
-            const bool ok = c < a.cache_cells;
+            const bool ok = c < a.cache_cells && QSA_IN((size_t)c * D + kh * 64 + 63, (size_t)a.cache_cells * D);
             const uint4 *src = reinterpret_cast<const uint4 *>(a.kq + (size_t)c * D + kh * 64);
 #pragma unroll
             for (int i = 0; i < 4; ++i) pre[i] = ok ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
@@ -294,7 +296,7 @@ __global__ void __maxnreg__(72) score_kernel(ScoreLaunch a) {
                 for (int it = 0; it < 2 * TN * 16 / PT; ++it) {
                     const int q = it * PT + pt, part = q / (TN * 16), r = (q / 16) % TN, u = q & 15;
                     const int t = w.tt * TN + r;
-                    const bool ok = t < a.ntok;
+                    const bool ok = t < a.ntok && QSA_IN(t, (a.ntok + 63) / 64 * 64);
                     cp_async16_zfill(dstB + part * PLANE + plane_off(r, u),
                                      reinterpret_cast<const uint4 *>(a.qsum + ((size_t)(ok ? t : 0) * 2 + part) * D) + u,
                                      ok ? 16u : 0u);
@@ -438,16 +440,22 @@ __global__ void __maxnreg__(72) score_kernel(ScoreLaunch a) {
                     for (int j = 0; j < 16; ++j, p += a.ld) {
                         const int c = j0 + j, t = tw + c;
                         const float f = exp2i(-__shfl_sync(0xffffffffu, (c & 1) ? ex.y : ex.x, c >> 1));
-                        if (full || (t < a.ntok && t >= tmin)) __stcs(p, fmaf(__uint_as_float(v[j]), inv, 0.0f) * f);
+                        if ((full || (t < a.ntok && t >= tmin)) && QSA_IN((size_t)t * a.ld + cell, (size_t)a.ntok * a.ld) &&
+                            QSA_IN(cell, a.ld))
+                            __stcs(p, fmaf(__uint_as_float(v[j]), inv, 0.0f) * f);
                     }
                 } else if (full) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j, p += a.ld) __stcs(p, fmaf(__uint_as_float(v[j]), inv, 0.0f));
+                    for (int j = 0; j < 16; ++j, p += a.ld)
+                        if (QSA_IN((size_t)(tw + j0 + j) * a.ld + cell, (size_t)a.ntok * a.ld) && QSA_IN(cell, a.ld))
+                            __stcs(p, fmaf(__uint_as_float(v[j]), inv, 0.0f));
                 } else {
 #pragma unroll
                     for (int j = 0; j < 16; ++j, p += a.ld) {
                         const int t = tw + j0 + j;
-                        if (t < a.ntok && t >= tmin) __stcs(p, fmaf(__uint_as_float(v[j]), inv, 0.0f));
+                        if (t < a.ntok && t >= tmin && QSA_IN((size_t)t * a.ld + cell, (size_t)a.ntok * a.ld) &&
+                            QSA_IN(cell, a.ld))
+                            __stcs(p, fmaf(__uint_as_float(v[j]), inv, 0.0f));
                     }
                 }
             };
@@ -554,3 +562,6 @@ cudaError_t launch_score_noalloc(const ScoreLaunch &a, cudaStream_t s) {
 }
 
 }  // namespace qsa
+
+QSA_DEFINE_CHECK_READER(take_check_word_score)
+

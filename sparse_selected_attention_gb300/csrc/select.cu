@@ -42,6 +42,7 @@
 // that also holds a valid cell, and its outside cells are masked.
 #include <stdint.h>
 
+#include "check.cuh"
 #include "qsa.h"
 #include "qsa_internal.h"
 
@@ -196,7 +197,8 @@ __global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
     const int p = a.pos0 + t, n = p + 1;
 
     if (n <= a.budget) {  // every causal cell is selected
-        for (int c = tid; c < a.width; c += THREADS) out[c] = c < n ? c : -1;
+        for (int c = tid; c < a.width; c += THREADS)
+            if (QSA_IN((size_t)t * a.width + c, (size_t)a.ntok * a.width)) out[c] = c < n ? c : -1;
         return;
     }
     // Sink [0, fs), free [fs, fe), tail [tail_lo, p].
@@ -239,7 +241,9 @@ __global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int q = qb + u * THREADS;
-            if (q < q1) v[u] = __ldg(rowq + q);
+            if (q < q1 && QSA_IN((long long)t * a.ld - mis + 4 * q, (long long)a.ntok * a.ld) &&
+                QSA_IN((long long)t * a.ld - mis + 4 * q + 3, (long long)a.ntok * a.ld))
+                v[u] = __ldg(rowq + q);
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
@@ -275,6 +279,7 @@ __global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
         clear_hist(sm);
         __syncthreads();
         for (int c = fs + tid; c < fe; c += THREADS) {
+            if (!QSA_IN(c, a.ld)) continue;
             const unsigned long long k = composite(__ldg(row + c), c);
             if ((k & mask) == prefix) atomicAdd(&sm.hist[(k >> sh) & (NBIN - 1)], 1);
         }
@@ -371,13 +376,14 @@ __global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
             have_hist = cnt > NFIN;
             for (int i = tid; i < nc; i += THREADS) {
                 const int c = cidx[i];
-                const unsigned long long k = composite(__ldg(row + c), c);
+                const unsigned long long k = QSA_IN(c, a.ld) ? composite(__ldg(row + c), c) : 0ull;
                 sm.cand[i] = k;
                 if (have_hist) atomicAdd(&sm.hist[(k >> 23) & (NBIN - 1)], 1);
             }
         }
     } else {
         for (int c = fs + tid; c < fe; c += THREADS) {
+            if (!QSA_IN(c, a.ld)) continue;
             const unsigned long long k = composite(__ldg(row + c), c);
             const unsigned long long km = k & mask;
             const int s = c + mis;
@@ -459,7 +465,8 @@ __global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
     int pos = scan_words(sm, sm.bits, w0, w1, wv, nbits);
 #pragma unroll
     for (int i = 0; i < 3; ++i)
-        for (unsigned m = wv[i]; m && pos < nsel; m &= m - 1u) out[fs + pos++] = 32 * (wb + i) + __ffs(m) - 1 - mis;
+        for (unsigned m = wv[i]; m && pos < nsel; m &= m - 1u, ++pos)
+            if (QSA_IN(fs + pos, a.width)) out[fs + pos] = 32 * (wb + i) + __ffs(m) - 1 - mis;
 }
 
 }  // namespace
@@ -473,3 +480,6 @@ cudaError_t launch_select(const SelectLaunch &a, cudaStream_t s) {
 }
 
 }  // namespace qsa
+
+QSA_DEFINE_CHECK_READER(take_check_word_select)
+

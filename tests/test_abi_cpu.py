@@ -211,3 +211,9 @@ def test_fill_ids_even_rejects(L, args):
 def test_fill_ids_zero_tokens_is_a_no_op(L):
     assert L.qsa_fill_ids_even(0, 0, 64, 64, None, None) == _abi.QSA_OK
     assert L.qsa_fill_ids_decode(0, 0, 384, 64, 256, None, None) == _abi.QSA_OK
+
+
+def test_check_word_needs_the_check_build(L):
+    out = ctypes.c_uint(7)
+    assert L.qsa_check_word(ctypes.byref(out)) == _abi.QSA_ERR_UNSUPPORTED and out.value == 0
+    assert L.qsa_check_word(None) == _abi.QSA_ERR_INVALID_ARG
