@@ -572,6 +572,7 @@ __host__ __device__ constexpr int xch_bytes() {
 template <int NW, int NS, int S>
 __global__ void __launch_bounds__(NW * 32, QSA_ATTN_MINB) attn_staged_kernel(AttnLaunch a) {
     extern __shared__ __align__(16) uint8_t smem8[];
+    wait_for_previous_grid();  // launched as a programmatic dependent: inputs may come from the previous kernel
     constexpr int NP = NW / S;  // unit groups per CTA
     const int t = a.ntok - 1 - (int)blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
@@ -822,8 +823,7 @@ cudaError_t launch_staged(const AttnLaunch &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(attn_staged_kernel<NW, NS, S>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attn_staged_kernel<NW, NS, S><<<dim3(a.ntok, a.n_kv_heads), NW * 32, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(attn_staged_kernel<NW, NS, S>, dim3(a.ntok, a.n_kv_heads), dim3(NW * 32), smem, s, a);
 }
 
 template <int S>

@@ -49,6 +49,7 @@ constexpr int HPW = 3;
 
 __global__ void __launch_bounds__(384, 4) prep_kernel(PrepParams P) {
     const PrepLaunch &a = P.a;
+    allow_dependent_launch();  // a programmatic dependent may be scheduled once every CTA has started
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (t >= a.ntok) {  // padding rows of the score's head sum

@@ -67,6 +67,33 @@ struct FillIdsLaunch {
     int32_t *ids;     // [ntok, width]
 };
 
+// Launches `kernel` as a programmatic dependent of the previous kernel in the
+// stream: its CTAs may be scheduled while that kernel finishes, and each one
+// waits (griddepcontrol.wait, at its start) for that grid's completion and
+// memory before it reads anything.  With no such predecessor it runs as a
+// plain launch.
+template <class... Args, class... Params>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+#ifdef __CUDACC__
+// The two halves of a programmatic dependency (sm_90 and later).
+__device__ __forceinline__ void wait_for_previous_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+#endif
+
 // Longest score row (cells) the selection kernel holds on chip.
 constexpr int kSelectMaxCells = 32768;
 

@@ -224,6 +224,8 @@ __global__ void __maxnreg__(72) score_kernel(ScoreLaunch a) {
     volatile int *abort = reinterpret_cast<volatile int *>(gen + OFF_FLAG);
     volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gen + OFF_FLAG + 8);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    wait_for_previous_grid();  // launched as a programmatic dependent: the head sum may come from qsa_prep
+    allow_dependent_launch();
 
     if (tid == 0) {
         for (int i = 0; i < NA; ++i) {
@@ -510,8 +512,7 @@ cudaError_t launch_score(const ScoreLaunch &a, cudaStream_t s) {
     if (a.max_ctas > 0 && a.max_ctas < grid) grid = a.max_ctas;
     e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    score_kernel<<<grid, THREADS, SMEM_ALLOC, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(score_kernel, dim3(grid), dim3(THREADS), SMEM_ALLOC, s, a);
 }
 
 // --- allocation-free variant --------------------------------------------------

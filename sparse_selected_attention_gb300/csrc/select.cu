@@ -190,6 +190,8 @@ __device__ __forceinline__ void find_crossing(Smem &sm, int need) {
 
 __global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
+    wait_for_previous_grid();  // launched as a programmatic dependent: the scores may come from qsa_score
+    allow_dependent_launch();
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
     const int t = blockIdx.x, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -475,8 +477,7 @@ cudaError_t launch_select(const SelectLaunch &a, cudaStream_t s) {
     if (a.ntok == 0) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    select_kernel<<<a.ntok, THREADS, SMEM_BYTES, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(select_kernel, dim3(a.ntok), dim3(THREADS), SMEM_BYTES, s, a);
 }
 
 }  // namespace qsa
