@@ -16,24 +16,26 @@
 // Ranking by (score descending, id ascending) is ranking by one unique 47-bit
 // composite key, (order_key(score) << 15) | (32767 - id), so the selected free
 // cells are exactly those whose composite is >= the need-th largest, K*.  K*
-// is found by a most-significant-digit radix select with 12-bit digits
-// (shifts 35, 23, 11, 0).  One 512-thread CTA per token row, two per SM:
-//   1. the free cells are streamed once from HBM as aligned float4 quads; each
-//      cell's top digit goes into a 4096-bin histogram and into a 16-bit digit
-//      cache in shared memory; the bin where the count from the top reaches
-//      `need` fixes the first digit;
-//   2. from the digit cache alone, each thread builds its two 32-cell words
-//      of two bitmaps: free cells whose top digit beats the crossing bin
-//      (selected) and free cells in it (candidates, a few hundred for smooth
-//      scores); a block scan of the candidate counts ranks them in cell order
-//      and their scores are reloaded (from L2) into the list, one per thread;
+// is found by a most-significant-digit radix select: the 12-bit top digit
+// (bit 35), then 11-bit digits (bits 24, 13, 2) and the last two bits.  One
+// 256-thread CTA per token row with 42 KB of shared memory, four per SM:
+//   1. the free cells are streamed once from HBM as aligned float4 quads.  The
+//      block's largest top digit in the first batch of loads places a window
+//      of 256 top-digit values (223 below it, 32 above); each cell's top digit,
+//      clamped into the window, goes into a 256-bin histogram and, as one
+//      byte, into a digit cache in shared memory.  The bin where the count
+//      from the top reaches `need` fixes the first digit, unless it is a
+//      clamped end bin (the window missed: step 1b);
+//   2. from the digit cache alone, each thread builds 32-cell words of the
+//      selected bitmap (cells above the crossing bin) and appends the cells
+//      in it (candidates, a few hundred for smooth scores) to a list; their
+//      scores are then reloaded (from L2) as full keys;
 //   3. the remaining digits are resolved on that list, at most 32 survivors
-//      are ranked by brute force, and each owner adds its candidates >= K*
-//      to its selected words;
-//   4. a block scan of the selected words places the selected free ids.
-// When more than CAP cells share the top digit (plateaus, outliers), further
-// digits are first resolved by extra passes over the row, and step 2 then
-// compares full composite keys.
+//      are ranked by brute force, and the candidates >= K* join the bitmap;
+//   4. a block scan of the bitmap words places the selected free ids.
+// 1b. When the window missed or more than CAP cells share the top digit
+// (plateaus, outliers), digits are resolved by extra passes over the row, and
+// step 2 then compares full composite keys.
 //
 // Bit positions are cell ids shifted by the row's misalignment `mis` (its
 // address modulo 16, in floats), so that quad q holds shifted cells 4q..4q+3,
@@ -49,36 +51,49 @@
 namespace qsa {
 namespace {
 
-constexpr int THREADS = 512;
+constexpr int THREADS = 256;
 constexpr int NWARP = THREADS / 32;
-constexpr int NBIN = 4096;            // 12-bit digits
-constexpr int BPT = NBIN / THREADS;   // bins per thread in the threshold scan
-constexpr int CAP = 2048;             // candidate list capacity
-constexpr int NFIN = 32;              // survivors ranked by brute force
+constexpr int WBINS = 256;                           // windowed top-digit bins
+constexpr int BELOW = 223;                           // window: [dmax - 223, dmax + 32]
+constexpr int CAP = 2048;                            // candidate list capacity
+constexpr int NFIN = 32;                             // survivors ranked by brute force
 constexpr int MAXQ = (kSelectMaxCells + 3 + 3) / 4;  // quads covering n + mis shifted cells
 constexpr int NWORD = (MAXQ + 7) / 8;                // bitmap words (8 quads each)
+constexpr int WPT = 4;                               // output scan: words per thread (the last thread 5)
+constexpr int SWEEP = 5;                             // sweep: words per thread at stride THREADS
 constexpr int UNROLL = 8;
-constexpr int NLEVEL = 4;
+constexpr int NLEVEL = 5;
+constexpr int RELOAD = CAP / THREADS;                // candidate reloads per thread
 static_assert(kSelectMaxCells <= 32768, "ids fit in 15 bits of the composite key");
-static_assert(NWORD <= 2 * THREADS + 1, "the output scan gives two words per thread, three to the last");
-static_assert(BPT == 8 && NBIN % 4 == 0, "two int4 loads per thread in the threshold scan");
+static_assert(NWORD <= WPT * THREADS + 1, "the output scan gives four words per thread, five to the last");
+static_assert(NWORD <= SWEEP * THREADS, "the sweep gives at most five words to a thread");
 
 __device__ __forceinline__ int level_shift(int level) {
-    return level == 0 ? 35 : level == 1 ? 23 : level == 2 ? 11 : 0;
+    return level == 0 ? 35 : level == 1 ? 24 : level == 2 ? 13 : level == 3 ? 2 : 0;
 }
+__device__ __forceinline__ int level_bins(int level) { return level == 0 ? 4096 : level == 4 ? 4 : 2048; }
 
 struct Smem {
-    int hist[NBIN];
-    unsigned long long cand[CAP];
+    // The digit cache while the row streams in; afterwards the histogram
+    // (first 16 KB) and the candidate keys (next 16 KB).
+    alignas(16) uint32_t dig[8 * NWORD];  // quad q's four windowed top digits, one byte each
+    uint16_t cidx[CAP];                   // candidate cells
+    int whist[WBINS];
     unsigned long long fin[NFIN];
     unsigned long long kstar;
     unsigned bits[NWORD + 7];
     int wtot[NWARP];
-    int cross[3];  // digit, count still needed inside it, cells in it
+    int cross[3];  // bin, count still needed inside it, cells in it
     int ncand, nfin;
-    alignas(16) uint2 dig[8 * NWORD];  // top digits of quad q's four cells, 16 bits each
 };
+static_assert(sizeof(int) * 4096 + sizeof(unsigned long long) * CAP <= sizeof(uint32_t) * 8 * NWORD,
+              "the histogram and the candidate keys fit in the digit cache");
 constexpr size_t SMEM_BYTES = sizeof(Smem);
+
+__device__ __forceinline__ int *hist_of(Smem &sm) { return reinterpret_cast<int *>(sm.dig); }
+__device__ __forceinline__ unsigned long long *cand_of(Smem &sm) {
+    return reinterpret_cast<unsigned long long *>(sm.dig + 4096);
+}
 
 // Order-preserving key; -0 and +0 are one value (they tie, lower id first).
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -93,6 +108,9 @@ __device__ __forceinline__ uint32_t top_digit(float f) {
     return (b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u)) >> 20;
 }
 
+// A top digit clamped into the window [base, base + 255], less base.
+__device__ __forceinline__ uint32_t window_bin(uint32_t d, int base) { return (uint32_t)min(max((int)d - base, 0), 255); }
+
 __device__ __forceinline__ unsigned long long composite(float x, int c) {
     return ((unsigned long long)order_key(x) << 15) | (unsigned)(32767 - c);
 }
@@ -106,13 +124,13 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
     return v;
 }
 
-// Bit e of the result is set iff the e-th of the four 12-bit digits packed in
-// (x, y) is >= thr, where c = 0x80008000 - (thr | thr << 16): each 16-bit lane
-// plus (0x8000 - thr) has bit 15 set exactly then, with no carry or borrow
-// between lanes.
-__device__ __forceinline__ uint32_t digits_ge(uint32_t x, uint32_t y, uint32_t c) {
-    const uint32_t gx = x + c, gy = y + c;
-    return ((gx >> 15) & 1u) | ((gx >> 30) & 2u) | ((gy >> 13) & 4u) | ((gy >> 28) & 8u);
+// Bit e of the result is set iff byte e of x is >= thr (thr <= 256), where
+// c = 0x80008000 - (thr | thr << 16): each 16-bit lane holding one byte plus
+// (0x8000 - thr) has bit 15 set exactly then, with no carry between lanes.
+__device__ __forceinline__ uint32_t bytes_ge(uint32_t x, uint32_t c) {
+    const uint32_t e = (x & 0x00ff00ffu) + c, o = ((x >> 8) & 0x00ff00ffu) + c;
+    const uint32_t m = ((e >> 15) & 0x00010001u) | ((o >> 14) & 0x00020002u);
+    return (m | (m >> 14)) & 15u;
 }
 
 // Bits of bitmap word w that fall in the shifted-cell range [lo, hi).
@@ -125,15 +143,15 @@ __device__ __forceinline__ unsigned range_bits(int w, int lo, int hi) {
 }
 
 // Ranks of the set bits of bitmap words [wlo, whi) in cell order.  Thread tid
-// owns words wlo + 2 tid and wlo + 2 tid + 1 (the last thread a third one);
+// owns words wlo + 4 tid .. wlo + 4 tid + 3 (the last thread a fifth one);
 // returns the rank of its first set bit and the total over the block.
-__device__ __forceinline__ int scan_words(Smem &sm, const unsigned *bm, int wlo, int whi, unsigned (&wv)[3],
+__device__ __forceinline__ int scan_words(Smem &sm, const unsigned *bm, int wlo, int whi, unsigned (&wv)[WPT + 1],
                                           int &total) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wb = wlo + 2 * tid, we = min(tid == THREADS - 1 ? wb + 3 : wb + 2, whi);
+    const int wb = wlo + WPT * tid, we = min(tid == THREADS - 1 ? wb + WPT + 1 : wb + WPT, whi);
     int mine = 0;
 #pragma unroll
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < WPT + 1; ++i) {
         wv[i] = wb + i < we ? bm[wb + i] : 0u;
         mine += __popc(wv[i]);
     }
@@ -150,45 +168,45 @@ __device__ __forceinline__ int scan_words(Smem &sm, const unsigned *bm, int wlo,
     return incl - mine;
 }
 
-__device__ __forceinline__ void clear_hist(Smem &sm) {
-    int4 *h = reinterpret_cast<int4 *>(sm.hist);
-    for (int i = threadIdx.x; i < NBIN / 4; i += THREADS) h[i] = make_int4(0, 0, 0, 0);
+__device__ __forceinline__ void clear_hist(int *h, int nb) {
+    int4 *h4 = reinterpret_cast<int4 *>(h);
+    for (int i = threadIdx.x; i < nb / 4; i += THREADS) h4[i] = make_int4(0, 0, 0, 0);
 }
 
-// Scans hist from the top bin down and publishes (digit, need left inside it,
-// its count) for the digit where the running count reaches `need`.  Thread
-// tid owns bins NBIN-8(tid+1) .. NBIN-1-8tid, read as two int4.
-__device__ __forceinline__ void find_crossing(Smem &sm, int need) {
+// Scans the nb-bin histogram h from the top bin down and publishes (bin, need
+// left inside it, its count) for the bin where the running count reaches
+// `need`.  Thread tid owns the nb / THREADS bins (one, for nb < THREADS)
+// below bin nb - per * tid.
+__device__ __forceinline__ void find_crossing(Smem &sm, const int *h, int nb, int need) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int4 *h = reinterpret_cast<const int4 *>(sm.hist + NBIN - BPT * (tid + 1));
-    const int4 lo = h[0], hi = h[1];
-    const int cnt[BPT] = {hi.w, hi.z, hi.y, hi.x, lo.w, lo.z, lo.y, lo.x};  // descending bins
+    const int per = nb >= THREADS ? nb / THREADS : 1;
+    const int top = nb - per * tid;
     int s = 0;
-#pragma unroll
-    for (int i = 0; i < BPT; ++i) s += cnt[i];
+    if (top > 0)
+        for (int i = 1; i <= per; ++i) s += h[top - i];
     int incl = warp_incl_scan(s, lane);
     if (lane == 31) sm.wtot[warp] = incl;
     __syncthreads();
 #pragma unroll
     for (int w = 0; w < NWARP; ++w) incl += w < warp ? sm.wtot[w] : 0;
     const int excl = incl - s;
-    if (excl < need && incl >= need) {
+    if (top > 0 && excl < need && incl >= need) {
         int run = excl;
-#pragma unroll
-        for (int i = 0; i < BPT; ++i) {
-            if (run + cnt[i] >= need) {
-                sm.cross[0] = NBIN - 1 - BPT * tid - i;
+        for (int i = 1; i <= per; ++i) {
+            const int c = h[top - i];
+            if (run + c >= need) {
+                sm.cross[0] = top - i;
                 sm.cross[1] = need - run;
-                sm.cross[2] = cnt[i];
+                sm.cross[2] = c;
                 break;
             }
-            run += cnt[i];
+            run += c;
         }
     }
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
+__global__ void __launch_bounds__(THREADS, 4) select_kernel(SelectLaunch a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     wait_for_previous_grid();  // launched as a programmatic dependent: the scores may come from qsa_score
     allow_dependent_launch();
@@ -196,11 +214,12 @@ __global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
     const int t = blockIdx.x, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     int32_t *out = a.ids + (size_t)t * a.width;
+    [[maybe_unused]] const size_t ids_n = (size_t)a.ntok * a.width, row0 = (size_t)t * a.width;
     const int p = a.pos0 + t, n = p + 1;
 
     if (n <= a.budget) {  // every causal cell is selected
         for (int c = tid; c < a.width; c += THREADS)
-            if (QSA_IN((size_t)t * a.width + c, (size_t)a.ntok * a.width)) out[c] = c < n ? c : -1;
+            if (QSA_IN(row0 + c, ids_n)) out[c] = c < n ? c : -1;
         return;
     }
     // Sink [0, fs), free [fs, fe), tail [tail_lo, p].
@@ -213,9 +232,12 @@ __global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
     const int total = fs + nsel + (n - tail_lo);
 
     // Forced runs and padding go straight out.
-    for (int i = tid; i < fs; i += THREADS) out[i] = i;
-    for (int i = tid; i < n - tail_lo; i += THREADS) out[fs + nsel + i] = tail_lo + i;
-    for (int i = total + tid; i < a.width; i += THREADS) out[i] = -1;
+    for (int i = tid; i < fs; i += THREADS)
+        if (QSA_IN(row0 + i, ids_n)) out[i] = i;
+    for (int i = tid; i < n - tail_lo; i += THREADS)
+        if (QSA_IN(row0 + fs + nsel + i, ids_n)) out[fs + nsel + i] = tail_lo + i;
+    for (int i = total + tid; i < a.width; i += THREADS)
+        if (QSA_IN(row0 + i, ids_n)) out[i] = -1;
     if (need <= 0) return;
 
     const float *row = a.scores + (size_t)t * a.ld;
@@ -224,9 +246,10 @@ __global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
     const int sfs = fs + mis, sfe = fe + mis;  // shifted free range
     const int q0 = sfs >> 2, q1 = (sfe + 3) >> 2;
     const int w0 = sfs >> 5, w1 = (sfe + 31) >> 5;  // bitmap words of the free range
+    [[maybe_unused]] const long long cells_n = (long long)a.ntok * a.ld, row_at = (long long)t * a.ld - mis;
 
     for (int w = w0 + tid; w < w1; w += THREADS) sm.bits[w] = 0u;
-    clear_hist(sm);
+    for (int i = tid; i < WBINS; i += THREADS) sm.whist[i] = 0;
     if (tid == 0) {
         sm.ncand = 0;
         sm.nfin = 0;
@@ -235,60 +258,92 @@ __global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
         sm.cross[2] = 1;
         sm.kstar = ~0ull;
     }
-    __syncthreads();
 
-    // 1. Top-digit histogram and digit cache, one pass over the free quads.
-    for (int qb = q0 + tid; qb < q1; qb += THREADS * UNROLL) {
+    // 1. Windowed top-digit histogram and digit cache, one pass over the free
+    //    quads.  The first batch's largest top digit places the window (the
+    //    barrier there also publishes the clears above).
+    int base = 0;
+    for (int qb = q0; qb < q1; qb += THREADS * UNROLL) {
         float4 v[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int q = qb + u * THREADS;
-            if (q < q1 && QSA_IN((long long)t * a.ld - mis + 4 * q, (long long)a.ntok * a.ld) &&
-                QSA_IN((long long)t * a.ld - mis + 4 * q + 3, (long long)a.ntok * a.ld))
+            const int q = qb + u * THREADS + tid;
+            v[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (q < q1 && QSA_IN(row_at + max(4 * q, sfs), cells_n) && QSA_IN(row_at + min(4 * q + 3, sfe - 1), cells_n))
                 v[u] = __ldg(rowq + q);
+        }
+        if (qb == q0) {
+            uint32_t dm = 0u;
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int s0 = 4 * (qb + u * THREADS + tid);
+                const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (s0 + e >= sfs && s0 + e < sfe) dm = max(dm, top_digit(x[e]));
+            }
+            dm = __reduce_max_sync(0xffffffffu, dm);
+            if (lane == 0) sm.wtot[warp] = (int)dm;
+            __syncthreads();
+            int m = 0;
+#pragma unroll
+            for (int w = 0; w < NWARP; ++w) m = max(m, sm.wtot[w]);
+            base = min(max(m - BELOW, 0), 4096 - WBINS);
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int q = qb + u * THREADS;
+            const int q = qb + u * THREADS + tid;
             if (q < q1) {
-                const uint32_t d0 = top_digit(v[u].x), d1 = top_digit(v[u].y);
-                const uint32_t d2 = top_digit(v[u].z), d3 = top_digit(v[u].w);
+                const uint32_t d0 = window_bin(top_digit(v[u].x), base), d1 = window_bin(top_digit(v[u].y), base);
+                const uint32_t d2 = window_bin(top_digit(v[u].z), base), d3 = window_bin(top_digit(v[u].w), base);
                 const int s0 = 4 * q;
                 if (s0 >= sfs && s0 + 4 <= sfe) {
-                    atomicAdd(&sm.hist[d0], 1);
-                    atomicAdd(&sm.hist[d1], 1);
-                    atomicAdd(&sm.hist[d2], 1);
-                    atomicAdd(&sm.hist[d3], 1);
+                    atomicAdd(&sm.whist[d0], 1);
+                    atomicAdd(&sm.whist[d1], 1);
+                    atomicAdd(&sm.whist[d2], 1);
+                    atomicAdd(&sm.whist[d3], 1);
                 } else {
-                    if (s0 >= sfs && s0 < sfe) atomicAdd(&sm.hist[d0], 1);
-                    if (s0 + 1 >= sfs && s0 + 1 < sfe) atomicAdd(&sm.hist[d1], 1);
-                    if (s0 + 2 >= sfs && s0 + 2 < sfe) atomicAdd(&sm.hist[d2], 1);
-                    if (s0 + 3 >= sfs && s0 + 3 < sfe) atomicAdd(&sm.hist[d3], 1);
+                    if (s0 >= sfs && s0 < sfe) atomicAdd(&sm.whist[d0], 1);
+                    if (s0 + 1 >= sfs && s0 + 1 < sfe) atomicAdd(&sm.whist[d1], 1);
+                    if (s0 + 2 >= sfs && s0 + 2 < sfe) atomicAdd(&sm.whist[d2], 1);
+                    if (s0 + 3 >= sfs && s0 + 3 < sfe) atomicAdd(&sm.whist[d3], 1);
                 }
-                sm.dig[q] = make_uint2(d0 | (d1 << 16), d2 | (d3 << 16));
+                sm.dig[q] = d0 | (d1 << 8) | (d2 << 16) | (d3 << 24);
             }
         }
     }
     __syncthreads();
-    find_crossing(sm, need);
-    unsigned long long prefix = (unsigned long long)sm.cross[0] << 35;
-    unsigned long long mask = (unsigned long long)(NBIN - 1) << 35;
-    int rem = sm.cross[1], cnt = sm.cross[2], level = 1;
+    find_crossing(sm, sm.whist, WBINS, need);
+    const int wbin = sm.cross[0];
+    // A clamped end bin holds several top digits: the window missed.
+    const bool miss = (wbin == WBINS - 1 && base + WBINS < 4096) || (wbin == 0 && base > 0);
+    unsigned long long prefix = 0ull, mask = 0ull;
+    int rem = need, cnt = 0x7fffffff, level = 0;
+    if (!miss) {
+        prefix = (unsigned long long)(base + wbin) << 35;
+        mask = 0xfffull << 35;
+        rem = sm.cross[1];
+        cnt = sm.cross[2];
+        level = 1;
+    }
 
-    // More digits over the row while the prefix group overflows the list.
+    // 1b. More digits over the row while the prefix group overflows the list
+    //     (from the top digit when the window missed).
+    int *hist = hist_of(sm);
+    unsigned long long *cand = cand_of(sm);
     while (cnt > CAP && level < NLEVEL) {
-        const int sh = level_shift(level);
-        clear_hist(sm);
+        const int sh = level_shift(level), nb = level_bins(level);
+        clear_hist(hist, nb);
         __syncthreads();
         for (int c = fs + tid; c < fe; c += THREADS) {
             if (!QSA_IN(c, a.ld)) continue;
             const unsigned long long k = composite(__ldg(row + c), c);
-            if ((k & mask) == prefix) atomicAdd(&sm.hist[(k >> sh) & (NBIN - 1)], 1);
+            if ((k & mask) == prefix) atomicAdd(&hist[(k >> sh) & (unsigned)(nb - 1)], 1);
         }
         __syncthreads();
-        find_crossing(sm, rem);
+        find_crossing(sm, hist, nb, rem);
         prefix |= (unsigned long long)sm.cross[0] << sh;
-        mask |= (unsigned long long)(NBIN - 1) << sh;
+        mask |= (unsigned long long)(nb - 1) << sh;
         rem = sm.cross[1];
         cnt = sm.cross[2];
         ++level;
@@ -297,91 +352,78 @@ __global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
     // 2. Free cells above the prefix set their bits; cells equal to it are
     //    candidates (with one such cell left, it is K* and simply selected).
     const bool collect = cnt > 1;
-    const bool fast = level == 1;  // only the top digit is fixed: work from the digit cache
-    bool have_hist = false;        // the histogram for `level` over the list is built
-    // Thread tid owns bitmap words wb .. wb + nown - 1 (two, the last thread
-    // three) of the free range.
-    const int wb = w0 + 2 * tid;
-    const int nown = max(0, min(tid == THREADS - 1 ? 3 : 2, w1 - wb));
-    uint32_t selw[3] = {0u, 0u, 0u}, eqw[3] = {0u, 0u, 0u};
-    int epos = 0;  // rank of the thread's first candidate in the list
+    const bool fast = !miss && level == 1;  // only the top digit is fixed: work from the digit cache
+    bool have_hist = false;                 // the histogram for `level` over the list is built
     if (fast) {
-        const uint32_t bs = sm.cross[0];
-        const uint32_t thr = bs + (collect ? 1u : 0u);  // selected: top digit >= thr
+        // Selected: window bin >= thr; candidates: window bin == wbin.  Words
+        // are dealt at stride THREADS; lanes 4..7 of each quarter warp read a
+        // word's halves in the other order, so a warp's 16-byte loads fall in
+        // distinct banks.
+        const uint32_t thr = (uint32_t)wbin + (collect ? 1u : 0u);  // <= 256
         const uint32_t c_sel = 0x80008000u - (thr | (thr << 16));
-        const uint32_t c_ge = 0x80008000u - (bs | (bs << 16));
-        clear_hist(sm);  // free since find_crossing; refilled by the reload below
-        // A word's 8 quads are 64 contiguous bytes of the cache; the two words
-        // are read as eight 16-byte pieces in a lane-rotated order so that a
-        // warp's loads spread over all banks.
+        const uint32_t c_eq = 0x80008000u - ((uint32_t)wbin | ((uint32_t)wbin << 16));
+        const int swap = (lane >> 2) & 1;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int r = (j + lane) & 7, wi = r >> 2, k = r & 3;
-            if (wi < nown) {
-                const uint4 v = reinterpret_cast<const uint4 *>(sm.dig + 8 * (wb + wi))[k];
-                const uint32_t g0 = digits_ge(v.x, v.y, c_sel), g1 = digits_ge(v.z, v.w, c_sel);
-                const uint32_t sb = (g0 | (g1 << 4)) << (8 * k);
-                uint32_t eb = 0u;
-                if (collect) {
-                    const uint32_t e0 = digits_ge(v.x, v.y, c_ge) & ~g0, e1 = digits_ge(v.z, v.w, c_ge) & ~g1;
-                    eb = (e0 | (e1 << 4)) << (8 * k);
+        for (int i = 0; i < SWEEP; ++i) {
+            const int w = w0 + tid + THREADS * i;
+            uint32_t sel = 0u, eq = 0u;
+            if (w < w1) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int h = hh ^ swap;
+                    const uint4 v = reinterpret_cast<const uint4 *>(sm.dig + 8 * w)[h];
+                    const uint32_t g[4] = {bytes_ge(v.x, c_sel), bytes_ge(v.y, c_sel), bytes_ge(v.z, c_sel),
+                                           bytes_ge(v.w, c_sel)};
+                    sel |= (g[0] | (g[1] << 4) | (g[2] << 8) | (g[3] << 12)) << (16 * h);
+                    if (collect) {
+                        const uint32_t e0 = bytes_ge(v.x, c_eq) & ~g[0], e1 = bytes_ge(v.y, c_eq) & ~g[1];
+                        const uint32_t e2 = bytes_ge(v.z, c_eq) & ~g[2], e3 = bytes_ge(v.w, c_eq) & ~g[3];
+                        eq |= (e0 | (e1 << 4) | (e2 << 8) | (e3 << 12)) << (16 * h);
+                    }
                 }
-                if (wi == 0) {
-                    selw[0] |= sb;
-                    eqw[0] |= eb;
-                } else {
-                    selw[1] |= sb;
-                    eqw[1] |= eb;
-                }
+                const unsigned vm = range_bits(w, sfs, sfe);
+                sel &= vm;
+                eq &= vm;
+                sm.bits[w] = sel;
+            }
+            if (collect) {
+                // Append the word's candidates: one shared atomic per warp.
+                const int nc = __popc(eq);
+                const int incl = warp_incl_scan(nc, lane);
+                int slot = 0;
+                if (lane == 31 && incl > 0) slot = atomicAdd(&sm.ncand, incl);
+                slot = __shfl_sync(0xffffffffu, slot, 31) + incl - nc;
+                for (uint32_t m = eq; m; m &= m - 1u, ++slot)
+                    if (slot < CAP) sm.cidx[slot] = (uint16_t)(32 * w + __ffs(m) - 1 - mis);
             }
         }
-        if (nown == 3) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint4 v = reinterpret_cast<const uint4 *>(sm.dig + 8 * (wb + 2))[k];
-                const uint32_t g0 = digits_ge(v.x, v.y, c_sel), g1 = digits_ge(v.z, v.w, c_sel);
-                selw[2] |= (g0 | (g1 << 4)) << (8 * k);
-                if (collect) {
-                    const uint32_t e0 = digits_ge(v.x, v.y, c_ge) & ~g0, e1 = digits_ge(v.z, v.w, c_ge) & ~g1;
-                    eqw[2] |= (e0 | (e1 << 4)) << (8 * k);
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 3; ++i) {
-            const uint32_t vm = i < nown ? range_bits(wb + i, sfs, sfe) : 0u;
-            selw[i] &= vm;
-            eqw[i] &= vm;
-        }
+        __syncthreads();  // the digit cache is dead: the histogram and the keys take its place
         if (collect) {
-            // Candidate ranks in cell order: a block scan of the owners' counts.
-            const int mine = __popc(eqw[0]) + __popc(eqw[1]) + __popc(eqw[2]);
-            int incl = warp_incl_scan(mine, lane);
-            if (lane == 31) sm.wtot[warp] = incl;
-            __syncthreads();
-#pragma unroll
-            for (int w = 0; w < NWARP; ++w) incl += w < warp ? sm.wtot[w] : 0;
-            epos = incl - mine;
-            // Candidate ids at their ranks, into the dead digit cache; then
-            // their full keys with one load per thread, all in flight at once
-            // (serial reloads by owners would each pay a loaded L2 round
-            // trip), building the next digit's histogram on the way.
-            int *cidx = reinterpret_cast<int *>(sm.dig);
-            int pos = epos;
-#pragma unroll
-            for (int i = 0; i < 3; ++i)
-                for (uint32_t m = eqw[i]; m; m &= m - 1u, ++pos)
-                    if (pos < CAP) cidx[pos] = 32 * (wb + i) + __ffs(m) - 1 - mis;
-            __syncthreads();
-            const int nc = min(cnt, CAP);
-            if (tid == 0) sm.ncand = nc;
+            const int nc = min(sm.ncand, CAP);
             have_hist = cnt > NFIN;
-            for (int i = tid; i < nc; i += THREADS) {
-                const int c = cidx[i];
-                const unsigned long long k = QSA_IN(c, a.ld) ? composite(__ldg(row + c), c) : 0ull;
-                sm.cand[i] = k;
-                if (have_hist) atomicAdd(&sm.hist[(k >> 23) & (NBIN - 1)], 1);
+            if (have_hist) {
+                clear_hist(hist, level_bins(1));
+                __syncthreads();
             }
+            // Every reload of the thread in flight at once (serial reloads
+            // would each pay a loaded L2 round trip).
+            float x[RELOAD];
+#pragma unroll
+            for (int j = 0; j < RELOAD; ++j) {
+                const int i = tid + THREADS * j;
+                const int c = i < nc ? (int)sm.cidx[i] : 0;
+                x[j] = (i < nc && QSA_IN(c, a.ld)) ? __ldg(row + c) : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < RELOAD; ++j) {
+                const int i = tid + THREADS * j;
+                if (i < nc) {
+                    const unsigned long long k = composite(x[j], sm.cidx[i]);
+                    cand[i] = k;
+                    if (have_hist) atomicAdd(&hist[(k >> 24) & 2047u], 1);
+                }
+            }
+            if (tid == 0) sm.ncand = nc;
         }
     } else {
         for (int c = fs + tid; c < fe; c += THREADS) {
@@ -392,7 +434,7 @@ __global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
             if (collect ? km > prefix : km >= prefix) atomicOr(&sm.bits[s >> 5], 1u << (s & 31));
             if (collect && km == prefix) {
                 const int slot = atomicAdd(&sm.ncand, 1);
-                if (slot < CAP) sm.cand[slot] = k;
+                if (slot < CAP) cand[slot] = k;
             }
         }
     }
@@ -402,26 +444,26 @@ __global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
     if (collect) {
         const int ncand = min(sm.ncand, CAP);
         while (cnt > NFIN && level < NLEVEL) {
-            const int sh = level_shift(level);
+            const int sh = level_shift(level), nb = level_bins(level);
             if (!have_hist) {
-                clear_hist(sm);
+                clear_hist(hist, nb);
                 __syncthreads();
                 for (int i = tid; i < ncand; i += THREADS) {
-                    const unsigned long long k = sm.cand[i];
-                    if ((k & mask) == prefix) atomicAdd(&sm.hist[(k >> sh) & (NBIN - 1)], 1);
+                    const unsigned long long k = cand[i];
+                    if ((k & mask) == prefix) atomicAdd(&hist[(k >> sh) & (unsigned)(nb - 1)], 1);
                 }
                 __syncthreads();
             }
             have_hist = false;
-            find_crossing(sm, rem);
+            find_crossing(sm, hist, nb, rem);
             prefix |= (unsigned long long)sm.cross[0] << sh;
-            mask |= (unsigned long long)(NBIN - 1) << sh;
+            mask |= (unsigned long long)(nb - 1) << sh;
             rem = sm.cross[1];
             cnt = sm.cross[2];
             ++level;
         }
         for (int i = tid; i < ncand; i += THREADS) {
-            const unsigned long long k = sm.cand[i];
+            const unsigned long long k = cand[i];
             if ((k & mask) == prefix) {
                 const int slot = atomicAdd(&sm.nfin, 1);
                 if (slot < NFIN) sm.fin[slot] = k;
@@ -437,38 +479,25 @@ __global__ void __launch_bounds__(THREADS, 2) select_kernel(SelectLaunch a) {
         }
         __syncthreads();
         const unsigned long long kstar = sm.kstar;
-        if (fast) {
-            // Each owner decides its own candidates, found at its ranks.
-            int pos = epos;
-#pragma unroll
-            for (int i = 0; i < 3; ++i)
-                for (uint32_t m = eqw[i]; m; m &= m - 1u, ++pos)
-                    if (pos < CAP && sm.cand[pos] >= kstar) selw[i] |= 1u << (__ffs(m) - 1);
-        } else {
-            for (int i = tid; i < ncand; i += THREADS) {
-                const unsigned long long k = sm.cand[i];
-                if (k >= kstar) {
-                    const int s = 32767 - (int)(k & 32767u) + mis;
-                    atomicOr(&sm.bits[s >> 5], 1u << (s & 31));
-                }
+        for (int i = tid; i < ncand; i += THREADS) {
+            const unsigned long long k = cand[i];
+            if (k >= kstar) {
+                const int s = 32767 - (int)(k & 32767u) + mis;
+                atomicOr(&sm.bits[s >> 5], 1u << (s & 31));
             }
-            __syncthreads();
         }
-    }
-    if (fast) {
-#pragma unroll
-        for (int i = 0; i < 3; ++i)
-            if (i < nown) sm.bits[wb + i] = selw[i];
+        __syncthreads();
     }
 
     // 4. Selected free ids, ascending, after the sink.
-    unsigned wv[3];
+    unsigned wv[WPT + 1];
     int nbits;
     int pos = scan_words(sm, sm.bits, w0, w1, wv, nbits);
+    const int wb = w0 + WPT * tid;
 #pragma unroll
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < WPT + 1; ++i)
         for (unsigned m = wv[i]; m && pos < nsel; m &= m - 1u, ++pos)
-            if (QSA_IN(fs + pos, a.width)) out[fs + pos] = 32 * (wb + i) + __ffs(m) - 1 - mis;
+            if (QSA_IN(row0 + fs + pos, ids_n)) out[fs + pos] = 32 * (wb + i) + __ffs(m) - 1 - mis;
 }
 
 }  // namespace
@@ -483,4 +512,3 @@ cudaError_t launch_select(const SelectLaunch &a, cudaStream_t s) {
 }  // namespace qsa
 
 QSA_DEFINE_CHECK_READER(take_check_word_select)
-

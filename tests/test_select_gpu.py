@@ -129,6 +129,23 @@ def test_select_degenerate_rows(cuda_device, kind):
     assert np.array_equal(run(sc, pos0), select_ids(sc, pos0))
 
 
+@pytest.mark.parametrize("kind", ["small_head", "huge_head", "negative"])
+def test_select_rows_far_from_their_first_cells(cuda_device, kind):
+    """Rows whose leading cells say little about the threshold: the first
+    9000 cells far smaller (or far larger) than the rest, and rows of
+    negative scores only.  A selection that sizes its first histogram from
+    the leading cells must still find the exact threshold."""
+    T, pos0 = 6, 20000
+    sc = wl.normal(78, 1, (T, pos0 + T)).astype(np.float32)
+    if kind == "small_head":
+        sc[:, :9000] *= np.float32(1e-6)
+    elif kind == "huge_head":
+        sc[:, :9000] *= np.float32(1e12)
+    else:
+        sc = -np.abs(sc) - np.float32(1.0)
+    assert np.array_equal(run(sc, pos0), select_ids(sc, pos0))
+
+
 @pytest.mark.parametrize("sink,local,budget", [(64, 256, 2048), (0, 5, 1000), (3, 0, 777)])
 def test_select_misaligned_rows(cuda_device, sink, local, budget):
     """An odd row stride puts row starts at every offset modulo 16 bytes."""
