@@ -15,7 +15,8 @@
 //
 // Ranking by (score descending, id ascending) is ranking by one unique 47-bit
 // composite key, (order_key(score) << 15) | (32767 - id), so the selected free
-// cells are exactly those whose composite is >= the need-th largest, K*.  K*
+// cells are exactly those whose composite is >= the need-th largest, K*.
+// NaN scores rank below every number (ties among them to the lower id).  K*
 // is found by a most-significant-digit radix select: the 12-bit top digit
 // (bit 35), then 11-bit digits (bits 24, 13, 2) and the last two bits.  One
 // 256-thread CTA per token row with 42 KB of shared memory, four per SM:
@@ -95,21 +96,20 @@ __device__ __forceinline__ unsigned long long *cand_of(Smem &sm) {
     return reinterpret_cast<unsigned long long *>(sm.dig + 4096);
 }
 
-// Order-preserving key; -0 and +0 are one value (they tie, lower id first).
+// Order-preserving key: -0 and +0 are one value (adding +0 turns -0 into +0),
+// and every NaN takes key 0, below -inf, so NaN scores rank last.
 __device__ __forceinline__ uint32_t order_key(float f) {
-    const uint32_t b = f == 0.0f ? 0u : __float_as_uint(f);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    const uint32_t b = __float_as_uint(f + 0.0f);
+    const uint32_t k = b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
+    return f != f ? 0u : k;
 }
 
-// order_key(f) >> 20 in integer operations.
-__device__ __forceinline__ uint32_t top_digit(float f) {
-    uint32_t b = __float_as_uint(f);
-    b = b == 0x80000000u ? 0u : b;
-    return (b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u)) >> 20;
-}
+__device__ __forceinline__ uint32_t top_digit(float f) { return order_key(f) >> 20; }
 
 // A top digit clamped into the window [base, base + 255], less base.
-__device__ __forceinline__ uint32_t window_bin(uint32_t d, int base) { return (uint32_t)min(max((int)d - base, 0), 255); }
+__device__ __forceinline__ uint32_t window_bin(uint32_t d, int base) {
+    return (uint32_t)min(__viaddmax_s32((int)d, -base, 0), 255);
+}
 
 __device__ __forceinline__ unsigned long long composite(float x, int c) {
     return ((unsigned long long)order_key(x) << 15) | (unsigned)(32767 - c);

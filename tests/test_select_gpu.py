@@ -146,6 +146,27 @@ def test_select_rows_far_from_their_first_cells(cuda_device, kind):
     assert np.array_equal(run(sc, pos0), select_ids(sc, pos0))
 
 
+def test_select_nan_and_infinite_scores(cuda_device):
+    """NaN scores (either sign, any payload) rank below every number, -inf
+    included, with ties among them going to the lower id; +inf ranks first."""
+    T, pos0 = 8, 5000
+    sc = wl.normal(79, 1, (T, pos0 + T)).astype(np.float32)
+    bits = sc.view(np.uint32)
+    bits[0, 100:4000] = 0x7FC00000                    # most of row 0 is NaN
+    bits[1, 100:4000:2] = 0xFFC00001                  # negative NaN with a payload
+    bits[1, 101:4000:2] = 0x7F800001                  # signalling NaN
+    sc[2, 300:700] = np.float32(np.inf)
+    sc[2, 700:4900] = np.float32(-np.inf)
+    bits[2, 900:1200] = 0x7FC00000
+    sc[3, :] = np.float32(-np.inf)
+    bits[3, 2000:2100] = 0xFFFFFFFF
+    bits[4, 64:4700:3] = 0x7FC00000                   # every third free cell NaN
+    got = run(sc, pos0)
+    with np.errstate(invalid="ignore"):  # the signalling NaNs, widened to float64
+        ref = select_ids(sc, pos0)
+    assert np.array_equal(got, ref)
+
+
 @pytest.mark.parametrize("sink,local,budget", [(64, 256, 2048), (0, 5, 1000), (3, 0, 777)])
 def test_select_misaligned_rows(cuda_device, sink, local, budget):
     """An odd row stride puts row starts at every offset modulo 16 bytes."""
