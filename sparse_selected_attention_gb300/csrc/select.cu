@@ -106,9 +106,17 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 __device__ __forceinline__ uint32_t top_digit(float f) { return order_key(f) >> 20; }
 
-// A top digit clamped into the window [base, base + 255], less base.
-__device__ __forceinline__ uint32_t window_bin(uint32_t d, int base) {
-    return (uint32_t)min(__viaddmax_s32((int)d, -base, 0), 255);
+// The float whose order key is k (k is not a NaN's key).
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// The window bin of f: f (a NaN taken as lo) is clamped into [lo, hi], the
+// numbers whose top digits are base .. base + 255, so its top digit less base
+// is the bin.
+__device__ __forceinline__ uint32_t window_bin(float f, float lo, float hi, int base) {
+    const uint32_t b = __float_as_uint(fminf(fmaxf(f + 0.0f, lo), hi));
+    return ((b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u)) >> 20) - (uint32_t)base;
 }
 
 __device__ __forceinline__ unsigned long long composite(float x, int c) {
@@ -290,12 +298,18 @@ __global__ void __launch_bounds__(THREADS, 4) select_kernel(SelectLaunch a) {
             for (int w = 0; w < NWARP; ++w) m = max(m, sm.wtot[w]);
             base = min(max(m - BELOW, 0), 4096 - WBINS);
         }
+        // lo is at least -FLT_MAX and hi at most +inf (keys below 0x00800000
+        // are -inf and negative NaNs, above 0xff800000 positive NaNs), so
+        // both are numbers and every bin lies in [0, 255]; a window that
+        // starts below -FLT_MAX counts as missed.
+        const float lo = key_float(max((uint32_t)base << 20, 0x00800000u));
+        const float hi = key_float(min(((uint32_t)(base + WBINS) << 20) - 1u, 0xff800000u));
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int q = qb + u * THREADS + tid;
             if (q < q1) {
-                const uint32_t d0 = window_bin(top_digit(v[u].x), base), d1 = window_bin(top_digit(v[u].y), base);
-                const uint32_t d2 = window_bin(top_digit(v[u].z), base), d3 = window_bin(top_digit(v[u].w), base);
+                const uint32_t d0 = window_bin(v[u].x, lo, hi, base), d1 = window_bin(v[u].y, lo, hi, base);
+                const uint32_t d2 = window_bin(v[u].z, lo, hi, base), d3 = window_bin(v[u].w, lo, hi, base);
                 const int s0 = 4 * q;
                 if (s0 >= sfs && s0 + 4 <= sfe) {
                     atomicAdd(&sm.whist[d0], 1);
@@ -316,7 +330,7 @@ __global__ void __launch_bounds__(THREADS, 4) select_kernel(SelectLaunch a) {
     find_crossing(sm, sm.whist, WBINS, need);
     const int wbin = sm.cross[0];
     // A clamped end bin holds several top digits: the window missed.
-    const bool miss = (wbin == WBINS - 1 && base + WBINS < 4096) || (wbin == 0 && base > 0);
+    const bool miss = (wbin == WBINS - 1 && base + WBINS < 4096) || (wbin == 0 && base > 0) || base < 8;
     unsigned long long prefix = 0ull, mask = 0ull;
     int rem = need, cnt = 0x7fffffff, level = 0;
     if (!miss) {

@@ -360,6 +360,18 @@ def test_select_signed_zeros_tie():
     assert ids[0].tolist() == [0, 2, 3, 7, -1, -1, -1, -1]
 
 
+def test_select_nan_ranks_last():
+    # A NaN score is no score: every number, -inf included, outranks it, and
+    # NaNs tie with each other (the lower id wins).  p = 9 with sink 1 and
+    # local 0 forces {0, 9}; budget 7 leaves five free slots among cells 1..8.
+    sc = np.zeros((1, 10), dtype=np.float32)
+    sc[0, 1:9] = [np.nan, -np.inf, np.nan, 1.0, np.nan, np.inf, -np.nan, -2.0]
+    with np.errstate(invalid="ignore"):
+        ids = select_ids(sc, pos0=9, width=8, budget=7, sink=1, local=0)
+    # free ranking: 6 (+inf), 4 (1.0), 8 (-2.0), 2 (-inf), then NaNs 1, 3, 5, 7
+    assert ids[0].tolist() == [0, 1, 2, 4, 6, 8, 9, -1]
+
+
 # ----------------------------------------------------------------------------
 # attention: output gate and several KV heads
 # ----------------------------------------------------------------------------
