@@ -152,6 +152,47 @@ def l2_copy_gbs(dev, nbytes=32 << 20, reps=200):
     return 2 * nbytes * reps / (e0.elapsed_time(e1) / 1e3) / 1e9
 
 
+def l2_gather_gbs(dev, reps=20):
+    """Measured L2 read rate for the attention's access pattern: 128-byte rows
+    gathered by id from an L2-resident 8.2 MB table (the K and V rows of the
+    long-context cache), eight lanes per row, over a grid that fills every SM
+    (libqsa_l2probe.so).  Row bytes plus id bytes per second; None if the
+    probe library was not built."""
+    import ctypes
+    import torch
+    from sparse_selected_attention_gb300 import build as qsa_build
+    if not os.path.exists(qsa_build.PROBE_LIB):
+        return None
+    L = ctypes.CDLL(qsa_build.PROBE_LIB)
+    L.qsa_l2_gather_probe.restype = ctypes.c_int
+    L.qsa_l2_gather_probe.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p, ctypes.c_longlong,
+                                      ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    nrows, nids = 2 * 31984, 2 * 1984 * 2048
+    g = torch.Generator(device=dev).manual_seed(7)
+    table = torch.randint(0, 255, (nrows * 128,), dtype=torch.uint8, device=dev, generator=g)
+    ids = torch.randint(0, nrows, (nids,), dtype=torch.int32, device=dev, generator=g)
+    blocks = 8 * torch.cuda.get_device_properties(dev).multi_processor_count
+    sink = torch.empty(blocks * 256, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+
+    def launch():
+        rc = L.qsa_l2_gather_probe(table.data_ptr(), nrows, ids.data_ptr(), nids, sink.data_ptr(), blocks, sp)
+        if rc != 0:
+            raise RuntimeError(f"qsa_l2_gather_probe failed ({rc})")
+
+    for _ in range(3):
+        launch()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(int(2e9 * 80e-6 * reps))  # the launches queue behind it and then run back to back
+    e0.record(stream)
+    for _ in range(reps):
+        launch()
+    e1.record(stream)
+    e1.synchronize()
+    return nids * (128 + 4) * reps / (e0.elapsed_time(e1) / 1e3) / 1e9
+
+
 def traffic_l2_record(kernel):
     """lts (L2) bytes per launch from the committed ncu summary, if current."""
     if traffic_record(kernel) is None:
@@ -555,11 +596,17 @@ def run_ours(args, rank, world, local_rank):
             "algorithmic_bytes_per_launch": alg[dom], "avg_launch_ms": avg[dom]}
     # The attention's gathers come from an L2-resident cache: its binding
     # roofline is L2 bandwidth.  lts bytes per launch (ncu) over the launch
-    # time, against a measured L2 copy rate.
-    l2peak = l2_copy_gbs(dev)
+    # time, against the L2 rate measured live for the same access pattern
+    # (128-byte rows by id); a device copy's rate is given beside it.
+    l2copy = l2_copy_gbs(dev)
+    l2gather = l2_gather_gbs(dev)
+    l2peak = l2gather if l2gather is not None else l2copy
     lts = traffic_l2_record(dom)
-    roof["l2"] = {"peak_gbs": l2peak, "peak_source": "measured live: 32 MiB device copy, L2-resident",
-                  "lts_bytes_per_launch": lts,
+    roof["l2"] = {"peak_gbs": l2peak,
+                  "peak_source": ("measured live: 128-byte rows gathered by id from an 8.2 MB L2-resident table, "
+                                  "row and id bytes" if l2gather is not None else
+                                  "measured live: 32 MiB device copy, L2-resident (gather probe not built)"),
+                  "copy_gbs": l2copy, "lts_bytes_per_launch": lts,
                   "achieved_gbs": None if lts is None else lts / (avg[dom] / 1e3) / 1e9,
                   "frac": None if lts is None else lts / (avg[dom] / 1e3) / 1e9 / l2peak,
                   "logical_frac": alg[dom] / (avg[dom] / 1e3) / 1e9 / l2peak}

@@ -13,6 +13,7 @@ built by build_all():
   libqsa_check.so  device-side index checks (QSA_CHECK=1): an index outside
                    its buffer sets a device word (read by qsa_check_word)
                    and the access is skipped.
+and libqsa_l2probe.so, the benchmark's L2 gather-rate probe.
 """
 from __future__ import annotations
 
@@ -122,12 +123,28 @@ def build_host_sanitized(verbose: bool = False) -> str:
     return lib
 
 
+PROBE_LIB = os.path.join(PKG, "libqsa_l2probe.so")
+
+
+def build_probe(verbose: bool = False, force: bool = False) -> str:
+    """libqsa_l2probe.so: the L2 gather-rate probe that the benchmark uses as
+    the attention's L2 roofline (not part of the attention path)."""
+    src = os.path.join(CSRC, "l2probe.cu")
+    if force or _stale(PROBE_LIB, [src]):
+        tmp = PROBE_LIB + ".tmp"
+        _run([nvcc(), *ARCH, "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", src, "-o", tmp], verbose)
+        os.replace(tmp, PROBE_LIB)
+    return PROBE_LIB
+
+
 def build_all(verbose: bool = False, force: bool = False) -> list:
-    """Every variant (release first), the variants in parallel."""
+    """Every variant (release first), the variants and the probe in parallel."""
     out = [build(verbose=verbose, force=force)]
     rest = [v for v in VARIANTS if v != "release"]
-    with ThreadPoolExecutor(max_workers=len(rest)) as ex:
-        out += list(ex.map(lambda v: build(verbose=verbose, force=force, variant=v), rest))
+    with ThreadPoolExecutor(max_workers=len(rest) + 1) as ex:
+        futs = [ex.submit(build, verbose=verbose, force=force, variant=v) for v in rest]
+        probe = ex.submit(build_probe, verbose=verbose, force=force)
+        out += [f.result() for f in futs] + [probe.result()]
     return out
 
 
