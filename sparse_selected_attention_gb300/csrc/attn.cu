@@ -744,6 +744,8 @@ __global__ void __launch_bounds__(NW * 32) attn_chunk_kernel(AttnLaunch a) {
     constexpr int NP = NW / S;
     constexpr int DR = D * S;
     __shared__ float xch[S == 2 ? NW * 2 * 16 * 32 : 1];
+    wait_for_previous_grid();  // launched as a programmatic dependent: q and ids may come from the kernel before
+    allow_dependent_launch();  // the merge may be scheduled; it waits for this grid's completion
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, r = lane & 3;
     const int pw = warp / S, half = warp % S;
@@ -784,13 +786,16 @@ __global__ void __launch_bounds__(NW * 32) attn_chunk_kernel(AttnLaunch a) {
     }
 }
 
-// Split path, part 2: max-first merge of the chunk partials of one token.
+// Split path, part 2: max-first merge of the chunk partials of one (token,
+// query head); a token's heads merge in parallel blocks (grid y, striding
+// when there are more heads than grid rows).
 template <int S>
 __global__ void __launch_bounds__(D * S) attn_merge_kernel(AttnLaunch a) {
     constexpr int DR = D * S;
+    wait_for_previous_grid();  // the chunk partials of the grid before
     const int t = blockIdx.x, d = threadIdx.x;
     const int nch = a.width / CHUNK;
-    for (int h = 0; h < a.n_q_heads; ++h) {
+    for (int h = blockIdx.y; h < a.n_q_heads; h += gridDim.y) {
         if (!QSA_IN(((size_t)t * nch * a.n_q_heads + h) * (DR + 2) + (size_t)(nch - 1) * a.n_q_heads * (DR + 2) + DR + 1,
                     (size_t)a.ntok * nch * a.n_q_heads * (DR + 2)))
             continue;
@@ -830,12 +835,11 @@ template <int S>
 cudaError_t launch_split(const AttnLaunch &a, cudaStream_t s) {
     constexpr int NW = 4;
     const int nch = a.width / CHUNK;
-    dim3 grid(a.ntok, a.n_kv_heads, (nch + NW / S - 1) / (NW / S));
-    attn_chunk_kernel<NW, S><<<grid, NW * 32, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    const dim3 grid(a.ntok, a.n_kv_heads, (nch + NW / S - 1) / (NW / S));
+    cudaError_t e = launch_dependent(attn_chunk_kernel<NW, S>, grid, dim3(NW * 32), 0, s, a);
     if (e != cudaSuccess) return e;
-    attn_merge_kernel<S><<<a.ntok, D * S, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(attn_merge_kernel<S>, dim3(a.ntok, a.n_q_heads < 65535 ? a.n_q_heads : 65535), dim3(D * S),
+                            0, s, a);
 }
 
 }  // namespace
