@@ -674,11 +674,12 @@ def _device_times(stream, fn, n, flush=None):
 def run_configs(dev, n):
     """Every workload the method is specified on, timed in the same run:
     the two decode windows (fused and split attention, L2 cold and warm),
-    the short and long prompt attention, and the score sweep."""
+    the short and long prompt attention, the score sweep, the selection over
+    the long-context scores and the attention at the pages' own shape."""
     import numpy as np
     import torch
 
-    from sparse_selected_attention_gb300 import qsa_attn, qsa_score, qsa_score_workspace_bytes
+    from sparse_selected_attention_gb300 import qsa_attn, qsa_score, qsa_score_workspace_bytes, qsa_select
     from sparse_selected_attention_gb300 import workloads as wl
 
     def to(x):
@@ -753,6 +754,46 @@ def run_configs(dev, n):
                       "tflops_head_summed_method": 2 * D * pairs / (ms / 1e3) / 1e12})
         del sc
     out["4_score_sweep"] = sweep
+
+    # The selection over the long-context scores (fp32 queries N(0,1) against
+    # the workload's key cache), then the attention at the pages' own shape.
+    w = wl.PROMPT_LONG
+    T, pos0, C = w.ntok, w.pos0, w.cells
+    cache = wl.make_cache(C, seed=5)
+    kq, ksc = to(cache.kq), to(cache.ksc)
+    sc = torch.empty((T, C), dtype=torch.float32, device=dev)
+    ws = torch.empty(qsa_score_workspace_bytes(T), dtype=torch.uint8, device=dev)
+    qsa_score(to(wl.queries_f32(T, seed=5)), kq, ksc, pos0, sc, ws)
+    ids = torch.empty((T, WIDTH), dtype=torch.int32, device=dev)
+    fn = lambda: qsa_select(sc, pos0, ids)
+    for _ in range(3):
+        fn()
+    t = _device_times(stream, fn, n, flush)
+    ms = sum(t) / len(t)
+    nb = select_bytes(T, pos0)
+    out["5_selection"] = {"workload": f"qsa_select over the scores of T={T}, pos0={pos0} (budget {WIDTH}: 64 sink + "
+                                      "256 local + current + best free cells)",
+                          "us": 1e3 * ms, "tokens_per_s": T / (ms / 1e3), "algorithmic_bytes": nb,
+                          "gbs": nb / (ms / 1e3) / 1e9, "frac_of_hbm_peak": nb / (ms / 1e3) / 1e9 / hbm}
+    del sc, ws, ids
+    hq, hkv, d, grp = wl.PAGES_Q_HEADS, wl.PAGES_KV_HEADS, wl.PAGES_HEAD_DIM, wl.PAGES_GROUP
+    cache = wl.make_cache(C, seed=wl.PAGES_SEED, head_dim=d, group=grp, kv_heads=hkv)
+    kq, vq, ksc, vsc = (to(x) for x in (cache.kq, cache.vq, cache.ksc, cache.vsc))
+    q = to(wl.queries_f16(T, seed=wl.PAGES_SEED, heads=hq, head_dim=d))
+    ids_np = wl.even_ids(T, pos0, WIDTH)
+    ids = to(ids_np)
+    o = torch.empty((T, hq, d), dtype=torch.float16, device=dev)
+    fn = lambda: qsa_attn(q, kq, vq, ksc, vsc, ids, o, wl.PAGES_SCALE)
+    for _ in range(3):
+        fn()
+    t = _device_times(stream, fn, max(n // 4, 10), flush)
+    ms = sum(t) / len(t)
+    ab, valid = attn_bytes(ids_np, T, hkv=hkv, hq=hq, d=d)
+    out["6_pages_shape"] = {"workload": f"attention at the pages' shape: {hkv} KV heads x {hq} query heads, "
+                                        f"head_dim {d}, per-{grp} scales, T={T}, pos0={pos0}, {WIDTH} evenly spaced ids",
+                            "us": 1e3 * ms, "tokens_per_s": T / (ms / 1e3), "valid_cells": valid,
+                            "algorithmic_bytes": ab, "logical_gbs": ab / (ms / 1e3) / 1e9,
+                            "frac_of_hbm_peak": ab / (ms / 1e3) / 1e9 / hbm}
     return out
 
 
