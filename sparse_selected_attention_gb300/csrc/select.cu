@@ -302,8 +302,12 @@ __global__ void __launch_bounds__(THREADS, 4) select_kernel(SelectLaunch a) {
         // are -inf and negative NaNs, above 0xff800000 positive NaNs), so
         // both are numbers and every bin lies in [0, 255]; a window that
         // starts below -FLT_MAX counts as missed.
+        // hi is never -0 either (key 0x7fffffff): whichever zero fminf
+        // returned for (+0, -0), +0 would fall one bin past the window, so
+        // the smallest negative subnormal, the same top digit, stands in.
         const float lo = key_float(max((uint32_t)base << 20, 0x00800000u));
-        const float hi = key_float(min(((uint32_t)(base + WBINS) << 20) - 1u, 0xff800000u));
+        const uint32_t hik = min(((uint32_t)(base + WBINS) << 20) - 1u, 0xff800000u);
+        const float hi = key_float(hik == 0x7fffffffu ? 0x7ffffffeu : hik);
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int q = qb + u * THREADS + tid;

@@ -129,7 +129,7 @@ def test_select_degenerate_rows(cuda_device, kind):
     assert np.array_equal(run(sc, pos0), select_ids(sc, pos0))
 
 
-@pytest.mark.parametrize("kind", ["small_head", "huge_head", "negative"])
+@pytest.mark.parametrize("kind", ["small_head", "huge_head", "negative", "negative_tiny"])
 def test_select_rows_far_from_their_first_cells(cuda_device, kind):
     """Rows whose leading cells say little about the threshold: the first
     9000 cells far smaller (or far larger) than the rest, and rows of
@@ -141,8 +141,18 @@ def test_select_rows_far_from_their_first_cells(cuda_device, kind):
         sc[:, :9000] *= np.float32(1e-6)
     elif kind == "huge_head":
         sc[:, :9000] *= np.float32(1e12)
-    else:
+    elif kind == "negative":
         sc = -np.abs(sc) - np.float32(1.0)
+    else:
+        # Negative scores near -1e-37 whose largest order key has top digit
+        # 2015 (0x7df), so a 256-digit window reaching 32 digits above it ends
+        # just below +0; 500 zeros of both signs after the leading cells rank
+        # above every one of them.
+        v = np.array([~np.uint32((2015 << 20) | 0xFFFFF)], dtype=np.uint32).view(np.float32)[0]
+        sc = (v * (np.float32(1.0) + np.abs(sc))).astype(np.float32)
+        sc[:, 100] = v
+        sc[:, 12000:12500] = np.float32(0.0)
+        sc[:, 12000:12500:2] = np.float32(-0.0)
     assert np.array_equal(run(sc, pos0), select_ids(sc, pos0))
 
 
