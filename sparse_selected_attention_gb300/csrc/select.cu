@@ -132,14 +132,24 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
     return v;
 }
 
-// Bit e of the result is set iff byte e of x is >= thr (thr <= 256), where
-// c = 0x80008000 - (thr | thr << 16): each 16-bit lane holding one byte plus
-// (0x8000 - thr) has bit 15 set exactly then, with no carry between lanes.
-__device__ __forceinline__ uint32_t bytes_ge(uint32_t x, uint32_t c) {
-    const uint32_t e = (x & 0x00ff00ffu) + c, o = ((x >> 8) & 0x00ff00ffu) + c;
-    const uint32_t m = ((e >> 15) & 0x00010001u) | ((o >> 14) & 0x00020002u);
-    return (m | (m >> 14)) & 15u;
+// Bit 7 of byte e of the result is set iff byte e of x is >= t, where T
+// holds t (<= 255) in every byte: the low seven bits compare through one
+// subtraction that cannot borrow across bytes ((x | 0x80) - (t & 0x7f) >= 1),
+// and the top bits settle the rest.
+__device__ __forceinline__ uint32_t bytes_ge(uint32_t x, uint32_t T) {
+    const uint32_t d = (x | 0x80808080u) - (T & 0x7f7f7f7fu);
+    return ((x & ~T) | (~(x ^ T) & d)) & 0x80808080u;
 }
+
+// Bit 7 of byte e of the result is set iff byte e of x equals w, where W
+// holds w in every byte (an exact zero-byte test of x ^ W).
+__device__ __forceinline__ uint32_t bytes_eq(uint32_t x, uint32_t W) {
+    const uint32_t y = x ^ W;
+    return ~(((y & 0x7f7f7f7fu) + 0x7f7f7f7fu) | y) & 0x80808080u;
+}
+
+// Bit 7 of each byte, as bits 0..3.
+__device__ __forceinline__ uint32_t byte_flags(uint32_t f) { return ((f >> 7) * 0x01020408u) >> 24; }
 
 // Bits of bitmap word w that fall in the shifted-cell range [lo, hi).
 __device__ __forceinline__ unsigned range_bits(int w, int lo, int hi) {
@@ -377,9 +387,9 @@ __global__ void __launch_bounds__(THREADS, 4) select_kernel(SelectLaunch a) {
         // are dealt at stride THREADS; lanes 4..7 of each quarter warp read a
         // word's halves in the other order, so a warp's 16-byte loads fall in
         // distinct banks.
-        const uint32_t thr = (uint32_t)wbin + (collect ? 1u : 0u);  // <= 256
-        const uint32_t c_sel = 0x80008000u - (thr | (thr << 16));
-        const uint32_t c_eq = 0x80008000u - ((uint32_t)wbin | ((uint32_t)wbin << 16));
+        const uint32_t thr = (uint32_t)wbin + (collect ? 1u : 0u);  // <= 256; 256 selects none
+        const uint32_t T = (thr & 255u) * 0x01010101u, W = (uint32_t)wbin * 0x01010101u;
+        const bool none = thr > 255u;
         const int swap = (lane >> 2) & 1;
 #pragma unroll
         for (int i = 0; i < SWEEP; ++i) {
@@ -390,13 +400,15 @@ __global__ void __launch_bounds__(THREADS, 4) select_kernel(SelectLaunch a) {
                 for (int hh = 0; hh < 2; ++hh) {
                     const int h = hh ^ swap;
                     const uint4 v = reinterpret_cast<const uint4 *>(sm.dig + 8 * w)[h];
-                    const uint32_t g[4] = {bytes_ge(v.x, c_sel), bytes_ge(v.y, c_sel), bytes_ge(v.z, c_sel),
-                                           bytes_ge(v.w, c_sel)};
-                    sel |= (g[0] | (g[1] << 4) | (g[2] << 8) | (g[3] << 12)) << (16 * h);
-                    if (collect) {
-                        const uint32_t e0 = bytes_ge(v.x, c_eq) & ~g[0], e1 = bytes_ge(v.y, c_eq) & ~g[1];
-                        const uint32_t e2 = bytes_ge(v.z, c_eq) & ~g[2], e3 = bytes_ge(v.w, c_eq) & ~g[3];
-                        eq |= (e0 | (e1 << 4) | (e2 << 8) | (e3 << 12)) << (16 * h);
+                    if (!none) {
+                        const uint32_t g = byte_flags(bytes_ge(v.x, T)) | (byte_flags(bytes_ge(v.y, T)) << 4) |
+                                           (byte_flags(bytes_ge(v.z, T)) << 8) | (byte_flags(bytes_ge(v.w, T)) << 12);
+                        sel |= g << (16 * h);
+                    }
+                    if (collect) {  // the crossing bin: disjoint from the selected bins above it
+                        const uint32_t e = byte_flags(bytes_eq(v.x, W)) | (byte_flags(bytes_eq(v.y, W)) << 4) |
+                                           (byte_flags(bytes_eq(v.z, W)) << 8) | (byte_flags(bytes_eq(v.w, W)) << 12);
+                        eq |= e << (16 * h);
                     }
                 }
                 const unsigned vm = range_bits(w, sfs, sfe);
