@@ -675,11 +675,12 @@ def run_configs(dev, n):
     """Every workload the method is specified on, timed in the same run:
     the two decode windows (fused and split attention, L2 cold and warm),
     the short and long prompt attention, the score sweep, the selection over
-    the long-context scores and the attention at the pages' own shape."""
+    the long-context scores, the attention at the pages' own shape, and prep
+    with and without the key rotation."""
     import numpy as np
     import torch
 
-    from sparse_selected_attention_gb300 import qsa_attn, qsa_score, qsa_score_workspace_bytes, qsa_select
+    from sparse_selected_attention_gb300 import qsa_attn, qsa_prep, qsa_score, qsa_score_workspace_bytes, qsa_select
     from sparse_selected_attention_gb300 import workloads as wl
 
     def to(x):
@@ -794,6 +795,25 @@ def run_configs(dev, n):
                             "us": 1e3 * ms, "tokens_per_s": T / (ms / 1e3), "valid_cells": valid,
                             "algorithmic_bytes": ab, "logical_gbs": ab / (ms / 1e3) / 1e9,
                             "frac_of_hbm_peak": ab / (ms / 1e3) / 1e9 / hbm}
+
+    # Prep on the long-context tokens, with and without the key rotation.
+    inp = wl.prep_inputs(T, seed=5)
+    qi, ki, vi, nw = (to(x) for x in (inp.q_in, inp.k_in, inp.v_in, inp.norm_w))
+    cache = wl.make_cache(C, seed=5)
+    kq, vq, ksc, vsc = (to(x) for x in (cache.kq, cache.vq, cache.ksc, cache.vsc))
+    q16 = torch.empty((T, HQ, D), dtype=torch.float16, device=dev)
+    ws = torch.empty(qsa_score_workspace_bytes(T), dtype=torch.uint8, device=dev)
+    rec = {"workload": f"qsa_prep of T={T} tokens at pos0={pos0} (12 query rows, one K and one V row each; "
+                       "the score's head sum written too)", "algorithmic_bytes": prep_bytes(T)}
+    for name, rk in (("plain", False), ("rope_k", True)):
+        fn = lambda: qsa_prep(qi, ki, vi, nw, pos0, kq, vq, ksc, vsc, q16, rope_k=rk, qbar_out=ws)
+        for _ in range(3):
+            fn()
+        t = _device_times(stream, fn, n, flush)
+        ms = sum(t) / len(t)
+        rec[name] = {"us": 1e3 * ms, "gbs": prep_bytes(T) / (ms / 1e3) / 1e9,
+                     "frac_of_hbm_peak": prep_bytes(T) / (ms / 1e3) / 1e9 / hbm}
+    out["7_prep"] = rec
     return out
 
 
