@@ -244,19 +244,22 @@ qsa_status qsa_score_noalloc(const qsa_score_args *args, void *stream);
  * the plainest reading.  For token t (p = pos0 + t):
  *   forced = {0 .. min(sink, p+1)-1} U {max(sink, p-local) .. p-1} U {p};
  *   the other causal cells c <= p are ranked by scores[t*ld + c] (float32,
- *   descending; equal scores, -0 and +0 included, rank the lower id first)
- *   and the best min(p+1, budget) - |forced| of them are added (none when
- *   the forced cells alone reach the budget: they are all kept);
+ *   descending; equal scores, -0 and +0 included, rank the lower id first;
+ *   a NaN ranks below every number, -inf included, NaNs among themselves by
+ *   id) and the best min(p+1, budget) - |forced| of them are added (none
+ *   when the forced cells alone reach the budget: they are all kept);
  *   ids[t, :] = the chosen cells ascending, then -1 up to width.
  * Deterministic and bit-exact for a given score array.
- * scores [ntok, ld] fp32 (only c <= p read; forced cells not at all);
- * ids [ntok, width] int32, every element written.  Both device pointers,
- * owned by the caller, 4-byte aligned.
+ * scores [ntok, ld] fp32: the ranked cells are read in aligned 16-byte
+ * blocks, so up to three neighbouring cells on either side (within those
+ * blocks) may be read too and are ignored; ids [ntok, width] int32, every
+ * element written.  Both device pointers, owned by the caller, 4-byte
+ * aligned.
  * Requires 1 <= budget <= width, width % 64 == 0, sink, local >= 0,
  * sink + local + 1 <= width and pos0 + ntok <= ld, else
  * QSA_ERR_INVALID_ARG; pos0 + ntok <= QSA_SELECT_MAX_CELLS (a row's top
  * digits are cached on chip), else QSA_ERR_UNSUPPORTED.  Nothing is
- * enqueued on an error.  Uses about 103 KB of shared memory per block and
+ * enqueued on an error.  Uses about 42 KB of shared memory per block and
  * no global scratch.
  */
 #define QSA_SELECT_MAX_CELLS 32768
