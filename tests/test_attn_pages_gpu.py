@@ -106,6 +106,20 @@ def test_pages_shape_long_context(cuda_device):
     assert_f16_close(out, ref, "pages shape, long context")
 
 
+def test_pages_shape_full_size_sampled(cuda_device):
+    """The bench's pages-shape workload in its own launch configuration: all
+    1984 tokens over 2048 evenly spaced ids of a 31984-cell cache, in one
+    call; 128 seeded rows plus the first and last compared with the oracle."""
+    T, pos0, W = 1984, 30000, 2048
+    cache = wl.make_cache(pos0 + T, seed=wl.PAGES_SEED, head_dim=D, group=GRP, kv_heads=HKV)
+    q = wl.queries_f16(T, seed=wl.PAGES_SEED, heads=H, head_dim=D)
+    ids = wl.even_ids(T, pos0, W)
+    out, _ = run(q, cache, ids, SCALE)
+    rows = np.unique(np.concatenate([[0, T - 1], np.argsort(wl.random_u64(wl.PAGES_SEED, 7, T), kind="stable")[:128]]))
+    ref, _, _, _ = attention(q[rows], cache.kq, cache.vq, cache.ksc, cache.vsc, ids[rows], SCALE, group=GRP)
+    assert_f16_close(out[rows], ref, "pages shape, full size, sampled rows")
+
+
 @pytest.mark.parametrize("part", [False, True])
 def test_gate_on_workload_shape(cuda_device, part):
     cache = wl.make_cache(5000, seed=43)
