@@ -40,6 +40,25 @@ def test_select_full_size_all_rows(cuda_device):
     assert not bad, f"{len(bad)} rows differ, first {bad[:5]}"
 
 
+def test_select_on_score_kernel_output_full_size(cuda_device):
+    """The bench's selection workload: qsa_score's own fp32 scores of 1984
+    tokens at pos0 30000 (fp32 queries N(0,1), the seed-5 key cache), then
+    qsa_select over them in one call; every row against select_ids on the
+    same scores."""
+    T, pos0 = 1984, 30000
+    C = pos0 + T
+    cache = wl.make_cache(C, seed=5)
+    sc = torch.empty((T, C), dtype=torch.float32, device="cuda")
+    ws = torch.empty(qsa_score_workspace_bytes(T), dtype=torch.uint8, device="cuda")
+    qsa_score(dev(wl.queries_f32(T, seed=5)), dev(cache.kq), dev(cache.ksc), pos0, sc, ws)
+    ids = torch.full((T, 2048), -7, dtype=torch.int32, device="cuda")
+    qsa_select(sc, pos0, ids)
+    torch.cuda.synchronize()
+    got, host = ids.cpu().numpy(), sc.cpu().numpy()
+    bad = [t for t in range(T) if not np.array_equal(got[t], select_ids(host[t:t + 1], pos0 + t)[0])]
+    assert not bad, f"{len(bad)} rows differ, first {bad[:5]}"
+
+
 def test_select_sample_misses_the_threshold(cuda_device):
     """Rows where every score inside 32 evenly spread runs of 32 cells is far
     below all others: a selection that estimated its threshold from such a
